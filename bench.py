@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark: masked attention forward + backward on one GB300 (N replicas
+under torchrun), effective TFLOP/s counting only attended score entries.
+
+Workload (the 8K static-mask sweep): batch 1, sequence 8192, 64 query heads /
+8 KV heads, head dim 128, bf16 Q, K, V, dO drawn i.i.d. N(0,1); one step runs
+forward + backward once per static mask family (12 masks; document families
+use seeded log-uniform document lengths over [128, 8192]).
+
+FLOPs: 4*d*nnz for the forward and 10*d*nnz for the backward, nnz = attended
+(query, key) cells summed over query heads, counted exactly on the device by
+lca_mask_nnz (checked against the oracle by the tests).
+
+Arms:
+  default            the CUDA library; prints one JSON line (rank 0)
+  --impl reference   the fp64 CPU oracle on the host cores, on a bounded sample
+                     of the same workload (rank 0 only)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "masked attn fwd+bwd effective TFLOP/s (unmasked FLOPs), % of GB300 BF16 peak"
+WORKLOAD = "static_mask_sweep_8k_gqa64x8_d128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_problems():
+    from gen import STATIC_KINDS, config2
+
+    return [config2(k) for k in STATIC_KINDS]
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(local_ms: float, local_units: float, world: int, device=None):
+    """(max time over ranks, sum of units over ranks).  Weak scaling: each
+    rank runs the full workload as a replica."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ oracle (CPU) sample
+def oracle_sample(kinds, heads=(0,)):
+    """Runs the oracle, as it stands, fwd + bwd on the given masks and query
+    heads of the workload; returns (effective flops, seconds)."""
+    import numpy as np
+
+    import oracle
+    from gen import config2, make_tensors
+
+    flops, secs = 0.0, 0.0
+    for kind in kinds:
+        prob = config2(kind)
+        q, k, v, do = make_tensors(prob)
+        G = prob.Hq // prob.Hkv
+        for h in heads:
+            g = h // G
+            qf = q[:, h:h + 1].float().numpy().astype(np.float64)
+            dof = do[:, h:h + 1].float().numpy().astype(np.float64)
+            kf = k[:, g:g + 1].float().numpy().astype(np.float64)
+            vf = v[:, g:g + 1].float().numpy().astype(np.float64)
+            from gen import Problem
+
+            p1 = Problem(prob.name, prob.Tq, prob.Tk, 1, 1, prob.d, prob.segments, prob.mask, prob.seed)
+            nnz = int(oracle.mask_row_counts(p1, 0).sum())
+            t0 = time.perf_counter()
+            oracle.attention_forward(p1, qf, kf, vf)
+            oracle.attention_backward(p1, qf, kf, vf, dof)
+            secs += time.perf_counter() - t0
+            flops += 14.0 * prob.d * nnz
+    return flops, secs
+
+
+def run_oracle_subprocess(kinds, threads):
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    cmd = [sys.executable, os.path.abspath(__file__), "--_oracle_sample", ",".join(kinds)]
+    out = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
+    if out.returncode != 0:
+        raise RuntimeError(out.stderr[-2000:])
+    return json.loads(out.stdout.strip().splitlines()[-1])
+
+
+BASELINE_SAMPLE = ("CAUSAL", "SLIDING", "CAUSAL_DOC", "SHARED_QUESTION")
+
+
+def cpu_baseline(kinds=BASELINE_SAMPLE):
+    kinds = list(kinds)
+    threads = os.cpu_count() or 1
+    r = run_oracle_subprocess(kinds, threads)
+    return {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd, query head 0 (KV head 0), {len(kinds)} static masks at 8192 tokens "
+                      f"({r['seconds']:.1f} s, numpy BLAS threads={threads})"}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from gen import STATIC_KINDS
+
+    kinds = list(STATIC_KINDS)
+    per_step = 4  # masks per step, round robin over the 12
+    threads = os.cpu_count() or 1
+    flops = secs = 0.0
+    for s in range(args.warmup + args.steps):
+        sel = [kinds[(s * per_step + i) % len(kinds)] for i in range(per_step)]
+        r = run_oracle_subprocess(sel, threads)
+        if s >= args.warmup:
+            flops += r["flops"]
+            secs += r["seconds"]
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": "query head 0, 4 static masks per step (round robin)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": "fp64 oracle fwd+bwd, query head 0, 4 of the 12 static masks per step at 8192 "
+                                   "tokens"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+
+    import long_context_masked_attention_gb300 as lca
+    from gen import make_tensors
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+
+    lca.load()
+    probs = workload_problems()
+    p0 = probs[0]
+    q, k, v, do = make_tensors(p0, device=dev)
+    calls = [lca.marshal(p.Tq, p.Tk, p.Hq, p.Hkv, p.d, p.segments, p.mask, p.scale) for p in probs]
+    ws_bytes = max(lca.workspace_size(c, True) for c in calls)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    nnz = [int(lca.mask_nnz(c).sum().item()) for c in calls]
+    d = p0.d
+    f_fwd = [4.0 * d * n for n in nnz]
+    f_bwd = [10.0 * d * n for n in nnz]
+    step_flops = sum(f_fwd) + sum(f_bwd)
+    o = torch.empty_like(q)
+    lse = torch.empty((p0.Hq, p0.Tq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(qq, kk, vv, dd, out_host=None):
+        for i, (p, c) in enumerate(zip(probs, calls)):
+            lca.attn_fwd(qq, kk, vv, p.segments, p.mask, p.scale, out=o, lse=lse, workspace=ws, call=c)
+            lca.attn_bwd(dd, qq, kk, vv, o, lse, p.segments, p.mask, p.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                         call=c)
+            if out_host is not None:
+                for src, dst in zip((o, lse, dq, dk, dv), out_host):
+                    dst.copy_(src, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step(q, k, v, do)
+    torch.cuda.synchronize()
+    st = lca.read_status(ws)
+    if st != (0, 0):
+        raise RuntimeError(f"device status after warm-up: {st}")
+
+    # ---- timed region: device-resident inputs, L2 flushed between steps
+    n_calls = 2 * len(probs) * args.steps
+    kev = lca.KernelEvents(4 * n_calls + 8)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").replace(",", "").isdigit() else local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = lca.launch_count()
+    kev.start()
+    for s in range(args.steps):
+        flush.zero_()
+        starts[s].record(stream)
+        step(q, k, v, do)
+        ends[s].record(stream)
+    kev.stop()
+    launches = lca.launch_count() - launches0
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    st = lca.read_status(ws)
+    if st != (0, 0):
+        raise RuntimeError(f"device status after timed region: {st}")
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    local_ms = sum(step_ms)
+    tot_ms, tot_flops = aggregate(local_ms, step_flops * args.steps, world, dev)
+    value = tot_flops / (tot_ms * 1e-3) / 1e12
+    phases = kev.durations()
+
+    # ---- end to end: pinned host inputs and outputs, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+        outs = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, dq, dk, dv)]
+        dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(t) for t in (q, k, v, do))
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = len(probs) * sum(t.numel() * t.element_size() for t in outs)
+        e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for s in range(args.steps):
+            flush.zero_()
+            e_s[s].record(stream)
+            for src, dst in zip((hq, hk, hv, hdo), (dq_in, dk_in, dv_in, ddo_in)):
+                dst.copy_(src, non_blocking=True)
+            step(dq_in, dk_in, dv_in, ddo_in, out_host=outs)
+            e_e[s].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms, e_flops = aggregate(sum(a.elapsed_time(b) for a, b in zip(e_s, e_e)), step_flops * args.steps, world,
+                                  dev)
+        e2e = {"value": e_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    pk, pk_src = peaks()
+    # dominant kernel and its roofline (algorithmic FLOPs per launch / launch time)
+    alg = {"fwd": 4.0, "dkv": 8.0, "dq": 6.0}  # executed matmul FLOPs per attended cell / d
+    kern = {ph: sum(v) for ph, v in phases.items() if ph in alg}
+    dom = max(kern, key=kern.get) if kern else None
+    roofline = None
+    if dom:
+        n_launch = len(phases[dom])
+        flops_dom = alg[dom] * d * sum(nnz) * args.steps
+        achieved = flops_dom / (sum(phases[dom]) * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
+                    "launches": n_launch, "peak_source": f"{pk_src} sustained bf16"}
+    phase_ms = {ph: sum(v) / args.steps for ph, v in phases.items()}
+    per_mask = {}
+    for p, n, ff, fb in zip(probs, nnz, f_fwd, f_bwd):
+        per_mask[p.mask.kind] = {"nnz": n}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; seeded document lengths)",
+        "config": {"workload": WORKLOAD, "seq_len": 8192, "batch": 1, "heads": "64:8", "head_dim": 128,
+                   "masks": [p.mask.kind for p in probs], "l2": "flushed between steps (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * value / pk["bf16_tflops_sustained"],
+        "peak_tflops": pk["bf16_tflops_sustained"], "peak_source": f"{pk_src} bf16 sustained",
+        "roofline": roofline, "phase_ms_per_step": phase_ms, "gpu_launches": launches,
+        "clocks": clk, "e2e": e2e, "per_mask_nnz": per_mask,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = cpu_baseline()
+        except Exception as exc:  # noqa: BLE001
+            line["cpu_baseline"] = {"value": None, "error": str(exc)[:200]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--_oracle_sample", default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args(argv)
+    if args._oracle_sample is not None:
+        flops, secs = oracle_sample(args._oracle_sample.split(","))
+        print(json.dumps({"flops": flops, "seconds": secs}))
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+/* lca_attn.h — C ABI of the GB300 (sm_103a) masked core-attention library.
+ *
+ * What it computes.  Core attention softmax(Q K^T * scale) V, forward and
+ * backward, as defined on the FlashAttention review page
+ * ("长上下文能力：FlashAttention vs. RingAttention", FlashAttention-1
+ * 问题和瓶颈), computed IO-aware (FlashAttention-1 核心优化: tiling, online
+ * softmax, fusion; FlashAttention-2 核心优化: deferred rescaling, one stored
+ * row statistic, sequence-parallel work split), under the mask families of
+ * the LongCA-bench review ("Long-Context Attention Benchmark", 三 技术架构,
+ * 掩码模式分类), over packed batches of token-level shards of arbitrary
+ * length ("Efficient Long-context Language Model Training by Core Attention
+ * Disaggregation", 方法详解: stateless, composable core attention).
+ *
+ * Conventions shared by every entry point.
+ *  - Tensors are token-major packed, row-major, bf16 unless stated:
+ *      Q, O, dO, dQ : [Tq][Hq][d]        K, V, dK, dV : [Tk][Hkv][d]
+ *      LSE          : [Hq][Tq] float32, natural log; -inf for a row with no key
+ *    d must be 128.  Query head h reads KV head h / (Hq / Hkv).
+ *  - Work is described by segments: query rows [q_off, q_off+q_len) attend
+ *    keys [k_off, k_off+k_len).  A plain batch is B equal segments, a
+ *    document-packed sequence one segment per document, a shard batch one
+ *    segment per shard with k_off = its document's start and k_len = the
+ *    shard's end within the document.  Causal families align the diagonal
+ *    bottom-right (query i sits at key position i + k_len - q_len).
+ *    Segments' query ranges must not overlap.  Segments with the same k_off
+ *    form a key group; different key groups' key ranges must not overlap.
+ *    Query rows outside every segment get O = 0, LSE = -inf, dQ = 0; keys
+ *    outside every segment get dK = dV = 0.
+ *  - The caller owns every buffer.  Pointers documented "device" are CUDA
+ *    device pointers; "host" pointers are read during the call only.  The
+ *    library allocates no device memory: it takes a caller-provided
+ *    workspace of at least lca_workspace_size() bytes, 256-byte aligned.
+ *  - Calls are asynchronous on `stream` and never synchronise, except
+ *    lca_read_status.  Argument errors are returned before anything is
+ *    launched.  Faults detected on the device (a bounded wait that ran out,
+ *    a block index out of range) are recorded in a status word inside the
+ *    workspace and read with lca_read_status.
+ */
+#ifndef LCA_ATTN_H
+#define LCA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LCA_API __attribute__((visibility("default")))
+#else
+#define LCA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LCA_OK = 0,
+  LCA_ERR_INVALID_ARG = 1, /* malformed shape, segments or mask descriptor   */
+  LCA_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels cover */
+  LCA_ERR_WORKSPACE = 3,   /* workspace null, misaligned or too small        */
+  LCA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed              */
+  LCA_ERR_TIMEOUT = 5,     /* device: a bounded pipeline wait ran out        */
+  LCA_ERR_DEVICE_ARG = 6   /* device: descriptor data out of range           */
+} lca_status;
+
+/* Mask families (LongCA-bench review, 三 技术架构, 掩码模式分类).  i and j are
+ * positions inside a segment, ie = i + k_len - q_len.  Readings of the
+ * unnamed details are stated per family. */
+typedef enum {
+  LCA_MASK_FULL = 0,             /* every key                                          */
+  LCA_MASK_CAUSAL = 1,           /* j <= ie                                            */
+  LCA_MASK_SLIDING = 2,          /* ie - window_left <= j <= ie + window_right          */
+  LCA_MASK_CAUSAL_SLIDING = 3,   /* ie - window_left <= j <= ie                         */
+  LCA_MASK_DOC = 4,              /* FULL inside each segment (segment = document)      */
+  LCA_MASK_CAUSAL_DOC = 5,       /* CAUSAL inside each segment                         */
+  LCA_MASK_SHARED_QUESTION = 6,  /* j <= ie and (part(j) == 0 or part(j) == part(ie));
+                                    part 0 = question, parts from part_bounds          */
+  LCA_MASK_GLOBAL_SLIDING = 7,   /* ie < num_global or j < num_global or
+                                    ie - window_left <= j <= ie + window_right          */
+  LCA_MASK_CAUSAL_BLOCKWISE = 8, /* j <= ie and (j/block == ie/block or
+                                    ie/block == (k_len-1)/block)                       */
+  LCA_MASK_PREFIX_LM_CAUSAL = 9, /* j < prefix_len or j <= ie                          */
+  LCA_MASK_PREFIX_LM_DOC = 10,   /* j < seg_prefix[segment] or j <= ie                 */
+  LCA_MASK_BLOCK_CAUSAL_DOC = 11,/* floor(j/block) <= floor(ie/block)                  */
+  LCA_MASK_BLOCK_SPARSE_UNIFORM = 12,  /* keep[h][qb][kb], blocks q_block x kv_block  */
+  LCA_MASK_BLOCK_SPARSE_VARIABLE = 13  /* keep[h][qb][kb], blocks from qb/kb_bounds    */
+} lca_mask_kind;
+
+typedef struct {
+  int32_t q_off, q_len, k_off, k_len;
+} lca_segment;
+
+typedef struct {
+  int32_t kind; /* lca_mask_kind */
+  int32_t window_left, window_right; /* inclusive distances, >= 0 */
+  int32_t num_global;                /* GLOBAL_SLIDING, >= 0 */
+  int32_t prefix_len;                /* PREFIX_LM_CAUSAL, >= 0 */
+  const int32_t* seg_prefix;         /* host [n_seg]: PREFIX_LM_DOC prefix per segment */
+  int32_t block;                     /* CAUSAL_BLOCKWISE, BLOCK_CAUSAL_DOC, >= 1 */
+  const int32_t* part_bounds;        /* host [n_part_bounds]: SHARED_QUESTION, strictly
+                                        increasing key positions, part_bounds[0] == 0,
+                                        last >= every segment's k_len, at most 64 */
+  int32_t n_part_bounds;
+  /* Block-sparse maps.  Block indices are over GLOBAL packed token positions
+   * (query row q_off+i, key k_off+j); the mask is also limited to the segment. */
+  int32_t q_block, kv_block;  /* UNIFORM: block sizes; kv_block >= 32            */
+  const int32_t* qb_bounds;   /* VARIABLE host [n_qb+1]: 0 = b0 < b1 < ... , b_last >= Tq */
+  const int32_t* kb_bounds;   /* VARIABLE host [n_kb+1]: every block but the last >= 32 */
+  int32_t n_qb, n_kb;         /* VARIABLE: block counts (UNIFORM: ignored)         */
+  int32_t heads_in_map;       /* 1 (one map for all heads) or Hq                   */
+  const int32_t* blk_row_ptr; /* device [heads_in_map*n_qb+1]: CSR row starts      */
+  const int32_t* blk_col_idx; /* device [blk_nnz]: kept kv block indices           */
+  int64_t blk_nnz;
+} lca_mask_desc;
+
+typedef struct {
+  int32_t Tq, Tk, Hq, Hkv, d;
+  int32_t n_seg;
+  const lca_segment* segs; /* host [n_seg] */
+  float scale;             /* softmax scale; 0 selects 1/sqrt(d) */
+} lca_shape;
+
+/* Bytes of workspace that lca_attn_fwd (for_bwd = 0) or lca_attn_bwd
+ * (for_bwd = 1) needs for this shape and mask; the same value serves
+ * lca_mask_materialize and lca_mask_nnz.  Host only; no CUDA call. */
+LCA_API lca_status lca_workspace_size(const lca_shape* shape, const lca_mask_desc* mask, int for_bwd, size_t* bytes);
+
+/* Forward (FlashAttention-2 核心优化: Q-split work, deferred rescale, one LSE
+ * per row).  q, k, v: device bf16 inputs; o: device bf16 [Tq][Hq][d] output;
+ * lse: device float [Hq][Tq] output. */
+LCA_API lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const lca_shape* shape,
+                        const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward (FlashAttention-2 核心优化, 反向传播: dK/dV per key tile, dQ in a
+ * separate query-tile pass, D = rowsum(dO * O) prepass).  dout, q, k, v, o:
+ * device bf16; lse: device float from lca_attn_fwd; dq, dk, dv: device bf16
+ * outputs (written, not accumulated). */
+LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
+                        const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Test hook: writes the mask of one segment and query head, evaluated by the
+ * same device predicate the attention kernels apply, as bytes (1 = attend)
+ * into `out` (device, q_len*k_len, row-major). */
+LCA_API lca_status lca_mask_materialize(const lca_shape* shape, const lca_mask_desc* mask, int32_t head, int32_t seg,
+                                uint8_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Test hook: the tile classes (0 empty, 1 full, 2 partial) of one segment and
+ * query head for 128 x 128 tiles, written to `out` (device, nq*nk bytes,
+ * nq = ceil(q_len/128), nk = ceil(k_len/128)). */
+LCA_API lca_status lca_mask_tile_classes(const lca_shape* shape, const lca_mask_desc* mask, int32_t head, int32_t seg,
+                                 uint8_t* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Number of attended (query, key) cells per query head, summed over
+ * segments, written to `nnz` (device, uint64 [Hq]).  Used for the effective
+ * FLOP count 4*d*nnz (forward) and 10*d*nnz (backward). */
+LCA_API lca_status lca_mask_nnz(const lca_shape* shape, const lca_mask_desc* mask, uint64_t* nnz, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, then copies the device status word of the last
+ * call that used this workspace: out[0] = lca_status code (0 = none),
+ * out[1] = where it was raised.  Each fwd/bwd call clears it first. */
+LCA_API lca_status lca_read_status(const void* workspace, int32_t out[2], void* stream);
+
+/* Test hook: launches one block that waits on a barrier nothing arrives at,
+ * with a wait limit of `limit_ms`; it must record LCA_ERR_TIMEOUT in the
+ * workspace status word and exit. */
+LCA_API lca_status lca_probe_wait_timeout(void* workspace, size_t workspace_bytes, int32_t limit_ms, void* stream);
+
+/* Profiling hook.  With a non-null ring of CUDA events (cudaEvent_t handles
+ * passed as void*, n_events even), every later fwd/bwd call records one
+ * event pair around each of its phases, on its own stream, taking the next
+ * pair of the ring (the cursor restarts at each call of this function):
+ *   lca_attn_fwd: 0 = mask compiler + cost sort, 1 = forward kernel
+ *   lca_attn_bwd: 2 = D prepass, 3 = dK/dV lists + sort, 4 = dK/dV kernel,
+ *                 5 = dQ lists + sort, 6 = dQ kernel
+ * The phase of each recorded pair is written to `phases` (host, n_events/2
+ * entries, may be null).  Pass null to stop.  Process-wide, not thread-safe. */
+LCA_API lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases);
+
+/* Number of kernels this library has launched since it was loaded. */
+LCA_API uint64_t lca_launch_count(void);
+
+LCA_API const char* lca_status_string(lca_status status);
+LCA_API int32_t lca_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LCA_ATTN_H */

@@ -1,0 +1,335 @@
+"""Thin ctypes binding of liblca_attn.so (include/lca_attn.h).
+
+Argument marshalling only: it builds the C structs, allocates outputs and the
+workspace with PyTorch when the caller does not pass them, and calls the
+library on the current CUDA stream.  Every step of the attention path runs in
+the library's kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass, field
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "liblca_attn.so")
+
+MASK_KINDS = (
+    "FULL", "CAUSAL", "SLIDING", "CAUSAL_SLIDING", "DOC", "CAUSAL_DOC", "SHARED_QUESTION", "GLOBAL_SLIDING",
+    "CAUSAL_BLOCKWISE", "PREFIX_LM_CAUSAL", "PREFIX_LM_DOC", "BLOCK_CAUSAL_DOC", "BLOCK_SPARSE_UNIFORM",
+    "BLOCK_SPARSE_VARIABLE",
+)
+STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "LCA_ERR_WORKSPACE",
+          4: "LCA_ERR_CUDA", 5: "LCA_ERR_TIMEOUT", 6: "LCA_ERR_DEVICE_ARG"}
+EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
+            "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
+            "lca_status_string", "lca_version")
+PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
+
+
+class LcaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class Segment_t(C.Structure):
+    _fields_ = [("q_off", C.c_int32), ("q_len", C.c_int32), ("k_off", C.c_int32), ("k_len", C.c_int32)]
+
+
+class MaskDesc_t(C.Structure):
+    _fields_ = [
+        ("kind", C.c_int32),
+        ("window_left", C.c_int32), ("window_right", C.c_int32),
+        ("num_global", C.c_int32),
+        ("prefix_len", C.c_int32),
+        ("seg_prefix", C.POINTER(C.c_int32)),
+        ("block", C.c_int32),
+        ("part_bounds", C.POINTER(C.c_int32)),
+        ("n_part_bounds", C.c_int32),
+        ("q_block", C.c_int32), ("kv_block", C.c_int32),
+        ("qb_bounds", C.POINTER(C.c_int32)), ("kb_bounds", C.POINTER(C.c_int32)),
+        ("n_qb", C.c_int32), ("n_kb", C.c_int32),
+        ("heads_in_map", C.c_int32),
+        ("blk_row_ptr", C.c_void_p), ("blk_col_idx", C.c_void_p),
+        ("blk_nnz", C.c_int64),
+    ]
+
+
+class Shape_t(C.Structure):
+    _fields_ = [("Tq", C.c_int32), ("Tk", C.c_int32), ("Hq", C.c_int32), ("Hkv", C.c_int32), ("d", C.c_int32),
+                ("n_seg", C.c_int32), ("segs", C.POINTER(Segment_t)), ("scale", C.c_float)]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads the library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with long_context_masked_attention_gb300._build.build()")
+    lib = C.CDLL(path)
+    st = C.c_int
+    vp = C.c_void_p
+    lib.lca_workspace_size.argtypes = [C.POINTER(Shape_t), C.POINTER(MaskDesc_t), C.c_int, C.POINTER(C.c_size_t)]
+    lib.lca_attn_fwd.argtypes = [vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp, C.c_size_t, vp]
+    lib.lca_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp,
+                                 C.c_size_t, vp]
+    lib.lca_mask_materialize.argtypes = [C.POINTER(Shape_t), C.POINTER(MaskDesc_t), C.c_int32, C.c_int32, vp, vp,
+                                         C.c_size_t, vp]
+    lib.lca_mask_tile_classes.argtypes = lib.lca_mask_materialize.argtypes
+    lib.lca_mask_nnz.argtypes = [C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp, vp, C.c_size_t, vp]
+    lib.lca_read_status.argtypes = [vp, C.POINTER(C.c_int32), vp]
+    lib.lca_probe_wait_timeout.argtypes = [vp, C.c_size_t, C.c_int32, vp]
+    lib.lca_set_kernel_events.argtypes = [C.POINTER(C.c_void_p), C.c_int32, C.POINTER(C.c_int32)]
+    lib.lca_launch_count.restype = C.c_uint64
+    lib.lca_launch_count.argtypes = []
+    lib.lca_status_string.argtypes = [st]
+    lib.lca_status_string.restype = C.c_char_p
+    lib.lca_version.restype = C.c_int32
+    for name in EXPORTED:
+        if name not in ("lca_status_string", "lca_version", "lca_launch_count"):
+            getattr(lib, name).restype = st
+    _lib = lib
+    return lib
+
+
+# ------------------------------------------------------------------ descriptors
+@dataclass
+class Mask:
+    """Mask descriptor; attribute names match lca_mask_desc (any object with
+    these attributes is accepted too)."""
+    kind: str
+    window_left: int = 0
+    window_right: int = 0
+    num_global: int = 0
+    prefix_len: int = 0
+    seg_prefix: list | None = None
+    block: int = 0
+    part_bounds: list | None = None
+    q_block: int = 0
+    kv_block: int = 0
+    qb_bounds: np.ndarray | None = None
+    kb_bounds: np.ndarray | None = None
+    heads_in_map: int = 1
+    blk_row_ptr: object = None
+    blk_col_idx: object = None
+
+
+@dataclass
+class Call:
+    """Marshalled C arguments plus the Python objects they point into."""
+    shape: Shape_t
+    mask: MaskDesc_t
+    keep: list = field(default_factory=list)
+
+
+def _i32(seq):
+    arr = np.ascontiguousarray(np.asarray(seq, dtype=np.int32))
+    return arr, arr.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale=0.0, device=None) -> Call:
+    """segments: iterable of objects with q_off/q_len/k_off/k_len or 4-tuples."""
+    import torch
+
+    segs = list(segments)
+    seg_arr = (Segment_t * max(1, len(segs)))()
+    for i, s in enumerate(segs):
+        if isinstance(s, (tuple, list)):
+            seg_arr[i] = Segment_t(*[int(x) for x in s])
+        else:
+            seg_arr[i] = Segment_t(int(s.q_off), int(s.q_len), int(s.k_off), int(s.k_len))
+    shape = Shape_t(int(Tq), int(Tk), int(Hq), int(Hkv), int(d), len(segs), seg_arr, float(scale))
+    md = MaskDesc_t()
+    keep = [seg_arr]
+    kind = mask.kind if isinstance(mask.kind, int) else MASK_KINDS.index(mask.kind)
+    md.kind = kind
+    md.window_left = int(getattr(mask, "window_left", 0) or 0)
+    md.window_right = int(getattr(mask, "window_right", 0) or 0)
+    md.num_global = int(getattr(mask, "num_global", 0) or 0)
+    md.prefix_len = int(getattr(mask, "prefix_len", 0) or 0)
+    md.block = int(getattr(mask, "block", 0) or 0)
+    if getattr(mask, "seg_prefix", None) is not None:
+        arr, ptr = _i32(mask.seg_prefix)
+        keep.append(arr)
+        md.seg_prefix = ptr
+    if getattr(mask, "part_bounds", None) is not None:
+        arr, ptr = _i32(mask.part_bounds)
+        keep.append(arr)
+        md.part_bounds = ptr
+        md.n_part_bounds = len(arr)
+    md.q_block = int(getattr(mask, "q_block", 0) or 0)
+    md.kv_block = int(getattr(mask, "kv_block", 0) or 0)
+    md.heads_in_map = int(getattr(mask, "heads_in_map", 1) or 1)
+    for name, cnt in (("qb_bounds", "n_qb"), ("kb_bounds", "n_kb")):
+        b = getattr(mask, name, None)
+        if b is not None:
+            arr, ptr = _i32(b)
+            keep.append(arr)
+            setattr(md, name, ptr)
+            setattr(md, cnt, len(arr) - 1)
+    rp = getattr(mask, "blk_row_ptr", None)
+    ci = getattr(mask, "blk_col_idx", None)
+    if rp is not None:
+        dev = device if device is not None else torch.device("cuda")
+
+        def to_dev(x):
+            if isinstance(x, torch.Tensor):
+                return x.to(device=dev, dtype=torch.int32).contiguous()
+            return torch.from_numpy(np.ascontiguousarray(np.asarray(x, dtype=np.int32))).to(dev)
+
+        trp, tci = to_dev(rp), to_dev(ci)
+        keep += [trp, tci]
+        md.blk_row_ptr = trp.data_ptr()
+        md.blk_col_idx = tci.data_ptr() if tci.numel() else None
+        md.blk_nnz = int(tci.numel())
+    return Call(shape, md, keep)
+
+
+def _check(code, what):
+    if code != 0:
+        raise LcaError(code, what)
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def workspace_size(call: Call, for_bwd: bool) -> int:
+    n = C.c_size_t(0)
+    _check(load().lca_workspace_size(C.byref(call.shape), C.byref(call.mask), int(for_bwd), C.byref(n)),
+           "lca_workspace_size")
+    return n.value
+
+
+def _workspace(call, for_bwd, workspace, device):
+    import torch
+
+    need = workspace_size(call, for_bwd)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    return workspace
+
+
+# ------------------------------------------------------------------ entry points
+def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=None, stream=None, call=None):
+    """q [Tq,Hq,128], k/v [Tk,Hkv,128] bf16 CUDA tensors -> (o, lse[Hq,Tq])."""
+    import torch
+
+    Tq, Hq, d = q.shape
+    Tk, Hkv, _ = k.shape
+    call = call or marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    workspace = _workspace(call, False, workspace, q.device)
+    _check(load().lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(), workspace.numel(),
+                               _stream(stream)), "lca_attn_fwd")
+    return out, lse
+
+
+def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, dv=None, workspace=None, stream=None,
+             call=None):
+    """Returns (dq, dk, dv) bf16."""
+    import torch
+
+    Tq, Hq, d = q.shape
+    Tk, Hkv, _ = k.shape
+    call = call or marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    workspace = _workspace(call, True, workspace, q.device)
+    _check(load().lca_attn_bwd(do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), C.byref(call.shape), C.byref(call.mask),
+                               workspace.data_ptr(), workspace.numel(), _stream(stream)), "lca_attn_bwd")
+    return dq, dk, dv
+
+
+def mask_materialize(call: Call, head: int, seg: int, q_len: int, k_len: int, device="cuda", stream=None):
+    import torch
+
+    out = torch.empty((q_len, k_len), dtype=torch.uint8, device=device)
+    ws = _workspace(call, False, None, device)
+    _check(load().lca_mask_materialize(C.byref(call.shape), C.byref(call.mask), head, seg, out.data_ptr(),
+                                       ws.data_ptr(), ws.numel(), _stream(stream)), "lca_mask_materialize")
+    return out
+
+
+def mask_tile_classes(call: Call, head: int, seg: int, q_len: int, k_len: int, device="cuda", stream=None):
+    import torch
+
+    nq, nk = -(-q_len // 128), -(-k_len // 128)
+    out = torch.empty((max(nq, 0), max(nk, 0)), dtype=torch.uint8, device=device)
+    ws = _workspace(call, False, None, device)
+    _check(load().lca_mask_tile_classes(C.byref(call.shape), C.byref(call.mask), head, seg, out.data_ptr(),
+                                        ws.data_ptr(), ws.numel(), _stream(stream)), "lca_mask_tile_classes")
+    return out
+
+
+def mask_nnz(call: Call, device="cuda", stream=None):
+    import torch
+
+    out = torch.zeros(call.shape.Hq, dtype=torch.int64, device=device)
+    ws = _workspace(call, False, None, device)
+    _check(load().lca_mask_nnz(C.byref(call.shape), C.byref(call.mask), out.data_ptr(), ws.data_ptr(), ws.numel(),
+                               _stream(stream)), "lca_mask_nnz")
+    return out
+
+
+def read_status(workspace, stream=None):
+    buf = (C.c_int32 * 2)()
+    _check(load().lca_read_status(workspace.data_ptr(), buf, _stream(stream)), "lca_read_status")
+    return int(buf[0]), int(buf[1])
+
+
+def probe_wait_timeout(workspace, limit_ms: int, stream=None):
+    _check(load().lca_probe_wait_timeout(workspace.data_ptr(), workspace.numel(), int(limit_ms), _stream(stream)),
+           "lca_probe_wait_timeout")
+
+
+class KernelEvents:
+    """Ring of CUDA event pairs the library records around each phase of its
+    fwd/bwd calls (lca_set_kernel_events)."""
+
+    def __init__(self, n_pairs: int):
+        import torch
+
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_pairs)]
+        self._arr = (C.c_void_p * (2 * n_pairs))(*[e.cuda_event for e in self.events])
+        self._ph = (C.c_int32 * n_pairs)(*([-1] * n_pairs))
+        self.n_pairs = n_pairs
+
+    def start(self):
+        for i in range(self.n_pairs):
+            self._ph[i] = -1
+        _check(load().lca_set_kernel_events(self._arr, 2 * self.n_pairs, self._ph), "lca_set_kernel_events")
+
+    def stop(self):
+        _check(load().lca_set_kernel_events(None, 0, None), "lca_set_kernel_events")
+
+    def durations(self):
+        """{phase name: [ms, ...]} for every recorded pair (call after a sync)."""
+        out = {}
+        for i in range(self.n_pairs):
+            ph = self._ph[i]
+            if ph < 0:
+                continue
+            out.setdefault(PHASES[ph], []).append(self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+        return out
+
+
+def launch_count() -> int:
+    return int(load().lca_launch_count())

@@ -1,0 +1,804 @@
+// lca_bwd.cu — masked attention backward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// The gradient of O = softmax(tau Q K^T) V (FlashAttention review page,
+// FlashAttention-2 核心优化, 反向传播), with P recomputed from the stored
+// row statistic LSE and D_i = dO_i . O_i from the prepass:
+//   dP = dO V^T,  dS = P * (dP - D),  dV = P^T dO,  dK = tau dS^T Q,
+//   dQ = tau dS K.
+// The page splits the backward both ways because dQ_i = sum_j dS_ij K_j
+// crosses key blocks.  Here that is two kernels, neither using atomics:
+//  * dkv_kernel — one work item per (KV head, key tile of 128 keys): it keeps
+//    K and V resident, walks every query head of the group and every 64-row
+//    query step that attends the tile (key-major list), and accumulates dV
+//    and dK in TMEM.  Per step: S^T = K Q^T and dP^T = V dO^T (TMEM),
+//    P^T, dS^T computed by 8 warps (thread = key row) and staged in shared
+//    memory, then dV += P^T dO and dK += dS^T Q.
+//  * dq_kernel — one work item per (query head, 128-row query tile): per key
+//    tile S = Q K^T, dP = dO V^T (TMEM), dS by 8 warps (thread = query row),
+//    then dQ += dS K.
+// Both are persistent (one CTA per SM), claim cost-sorted items through an
+// atomic counter, and use one TMA producer warp and one MMA-issue warp.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "lca_internal.h"
+#include "sm103.cuh"
+
+namespace lca {
+namespace {
+
+constexpr int kThreads = 320;  // 8 compute warps + MMA warp + TMA warp
+constexpr uint32_t kTile128 = 32768;  // 128 rows x 128 bf16
+constexpr uint32_t kChunk128 = 16384; // 128 rows x 64 bf16
+constexpr uint32_t kTile64 = 16384;   // 64 rows x 128 bf16
+constexpr uint32_t kChunk64 = 8192;   // 64 rows x 64 bf16
+constexpr uint32_t kIdesc128 = idesc_bf16_f32(128, 128, false, false);
+constexpr uint32_t kIdesc64 = idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t kIdescMN = idesc_bf16_f32(128, 128, false, true);
+
+__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const AttnArgs& a, int where) {
+  return mbar_wait(bar, parity, a.status, a.wait_limit_ns, kStatusTimeout, where);
+}
+__device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, const AttnArgs& a, int where) {
+  const bool ok = mbar_wait(bar, parity, a.status, a.wait_limit_ns, kStatusTimeout, where);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v, float mul) {
+  uint4 r;
+  r.x = pack_bf16x2(v[0] * mul, v[1] * mul);
+  r.y = pack_bf16x2(v[2] * mul, v[3] * mul);
+  r.z = pack_bf16x2(v[4] * mul, v[5] * mul);
+  r.w = pack_bf16x2(v[6] * mul, v[7] * mul);
+  return r;
+}
+
+// ====================================================================== dQ
+namespace dq {
+
+constexpr int kOffQ = 0;
+constexpr int kOffDO = kOffQ + kTile128;
+constexpr int kOffDS = kOffDO + kTile128;
+constexpr int kOffK = kOffDS + kTile128;  // 2-slot K ring
+constexpr int kOffV = kOffK + 2 * kTile128;  // 2-slot V ring
+constexpr int kOffCtl = kOffV + 2 * kTile128;
+constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
+
+enum : int {
+  B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1, B_VEMPTY, B_VEMPTY1,
+  B_SFULL, B_SEMPTY, B_DSFULL, B_DSEMPTY, B_DQFULL, B_ITFULL, B_ITFULL1, B_ITEMPTY, B_ITEMPTY1, B_DRAIN, B_COUNT
+};
+
+struct Item {
+  int valid, seg, qt, head, hm, cnt;
+  long long ebase;
+};
+
+__device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
+                                         const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
+                                         Item* items) {
+  const PlanView& pv = a.pv;
+  const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  uint32_t tiles = 0;  // key tiles loaded so far (K and V rings advance together)
+  uint32_t k_issued = 0, v_issued = 0;
+  int q_issued = 0;
+  int it = 0;
+  for (;; ++it) {
+    const int slot = it & 1;
+    if (it >= 2 && !wait1(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 110)) goto abort;
+    {
+      const int w = atomicAdd(a.counter, 1);
+      Item inf;
+      inf.valid = 0;
+      if (w < a.n_work) {
+        const int row = a.order[w / a.expand];
+        const int hm = row / pv.R128, rr = row % pv.R128;
+        const int s = find_bucket(pv.q128_start, pv.n_seg, rr);
+        inf.valid = 1;
+        inf.seg = s;
+        inf.qt = rr - pv.q128_start[s];
+        inf.hm = hm;
+        inf.head = (pv.hm_count == 1) ? (w % a.expand) : hm;
+        inf.cnt = a.cnt[row];
+        inf.ebase = hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(inf.qt) * pv.segs[s].nk;
+      }
+      items[slot] = inf;
+      mbar_arrive(&bar[B_ITFULL + slot]);
+      if (!inf.valid) return;
+      const SegInfo sg = pv.segs[inf.seg];
+      if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 111)) goto abort;
+      mbar_arrive_expect_tx(&bar[B_QFULL], 2 * kTile128);
+      const int y0 = sg.q_off + inf.qt * kTile;
+      for (int c = 0; c < 2; ++c) {
+        tma_load_2d(sm + kOffQ + c * kChunk128, tq, &bar[B_QFULL], inf.head * kHeadDim + c * 64, y0);
+        tma_load_2d(sm + kOffDO + c * kChunk128, tdo, &bar[B_QFULL], inf.head * kHeadDim + c * 64, y0);
+      }
+      q_issued = it + 1;
+      const int g = inf.head / pv.G;
+      for (int t = 0; t < inf.cnt; ++t, ++tiles) {
+        const int kt = static_cast<int>(entries[inf.ebase + t] & 0xFFFFFFu);
+        const int yk = sg.k_off + kt * kTile;
+        const int b = tiles & 1;
+        const uint32_t ph = ((tiles >> 1) - 1) & 1;
+        if (tiles >= 2 && !wait1(&bar[B_KEMPTY + b], ph, a, 112)) goto abort;
+        mbar_arrive_expect_tx(&bar[B_KFULL + b], kTile128);
+        tma_load_2d(sm + kOffK + b * kTile128, tk, &bar[B_KFULL + b], g * kHeadDim, yk);
+        tma_load_2d(sm + kOffK + b * kTile128 + kChunk128, tk, &bar[B_KFULL + b], g * kHeadDim + 64, yk);
+        k_issued = tiles + 1;
+        if (tiles >= 2 && !wait1(&bar[B_VEMPTY + b], ph, a, 113)) goto abort;
+        mbar_arrive_expect_tx(&bar[B_VFULL + b], kTile128);
+        tma_load_2d(sm + kOffV + b * kTile128, tv, &bar[B_VFULL + b], g * kHeadDim, yk);
+        tma_load_2d(sm + kOffV + b * kTile128 + kChunk128, tv, &bar[B_VFULL + b], g * kHeadDim + 64, yk);
+        v_issued = tiles + 1;
+      }
+    }
+  }
+abort:
+  for (uint32_t d = 0; d < 2 && d < k_issued; ++d) {
+    const uint32_t idx = k_issued - 1 - d;
+    mbar_wait(&bar[B_KFULL + (idx & 1)], (idx >> 1) & 1, nullptr, 100000000ull, 0, 0);
+  }
+  for (uint32_t d = 0; d < 2 && d < v_issued; ++d) {
+    const uint32_t idx = v_issued - 1 - d;
+    mbar_wait(&bar[B_VFULL + (idx & 1)], (idx >> 1) & 1, nullptr, 100000000ull, 0, 0);
+  }
+  if (q_issued >= 1) mbar_wait(&bar[B_QFULL], (q_issued - 1) & 1, nullptr, 100000000ull, 0, 0);
+}
+
+__device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items,
+                                           uint32_t tbase) {
+  const uint32_t base = smem_u32(sm);
+  const uint32_t q_addr = base + kOffQ, do_addr = base + kOffDO, ds_addr = base + kOffDS;
+  uint32_t tiles = 0;     // key tiles consumed (ring position)
+  uint32_t sdp = 0;       // S/dP products issued (TMEM reuse count)
+  uint32_t dsn = 0;       // dQ products issued (dS buffer reuse count)
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 120)) goto abort;
+    {
+      const Item inf = items[slot];
+      mbar_arrive(&bar[B_ITEMPTY + slot]);
+      if (!inf.valid) return;
+      if (!wait1(&bar[B_QFULL], it & 1, a, 121)) goto abort;
+      tc_fence_after();
+      const int n = inf.cnt;
+      for (int t = 0; t <= n; ++t) {
+        if (t < n) {  // S = Q K^T, dP = dO V^T for key tile t
+          const uint32_t idx = tiles + t;
+          const int b = idx & 1;
+          const uint32_t ph = (idx >> 1) & 1;
+          if (sdp >= 1 && !wait1(&bar[B_SEMPTY], (sdp - 1) & 1, a, 122)) goto abort;
+          if (!wait1(&bar[B_KFULL + b], ph, a, 123)) goto abort;
+          tc_fence_after();
+          const uint32_t k_addr = base + kOffK + b * kTile128;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
+            umma_ss(tbase + 0, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdesc128,
+                    ks > 0);
+          }
+          if (!wait1(&bar[B_VFULL + b], ph, a, 124)) goto abort;
+          tc_fence_after();
+          const uint32_t v_addr = base + kOffV + b * kTile128;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
+            umma_ss(tbase + 128, sdesc_sw128(do_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
+                    kIdesc128, ks > 0);
+          }
+          umma_commit(&bar[B_SFULL]);
+          umma_commit(&bar[B_VEMPTY + b]);
+          ++sdp;
+          if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
+        }
+        if (t >= 1) {  // dQ += dS K for key tile t-1
+          const uint32_t idx = tiles + t - 1;
+          const int b = idx & 1;
+          if (!wait1(&bar[B_DSFULL], dsn & 1, a, 125)) goto abort;
+          tc_fence_after();
+          const uint32_t k_addr = base + kOffK + b * kTile128;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t aoff = (ks >> 2) * kChunk128 + (ks & 3) * 32;
+            umma_ss(tbase + 256, sdesc_sw128(ds_addr + aoff, 16, 1024),
+                    sdesc_sw128(k_addr + ks * 2048, kChunk128, 1024), kIdescMN, (ks > 0 || t > 1) ? 1u : 0u);
+          }
+          umma_commit(&bar[B_DSEMPTY]);
+          umma_commit(&bar[B_KEMPTY + b]);
+          ++dsn;
+          if (t == n) umma_commit(&bar[B_DQFULL]);
+        }
+      }
+      if (n == 0) umma_commit(&bar[B_QEMPTY]);
+      tiles += n;
+    }
+  }
+abort:
+  umma_commit(&bar[B_DRAIN]);
+  mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
+}
+
+__device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
+  const PlanView& pv = a.pv;
+  const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  const int warp = threadIdx.x >> 5;
+  const int wq = warp & 3, half = warp >> 2;
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;
+  const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
+  const float sl2 = a.scale_log2;
+  uint8_t* sDS = sm + kOffDS + half * kChunk128;  // this thread's 64 key columns = one swizzle chunk
+  __nv_bfloat16* dQ = static_cast<__nv_bfloat16*>(a.dq);
+  uint32_t sdp = 0, dsn = 0, items_done = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 130)) return;
+    const Item inf = items[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
+    if (!inf.valid) return;
+    const SegInfo sg = pv.segs[inf.seg];
+    const int i = inf.qt * kTile + row;
+    const bool valid = i < sg.q_len;
+    const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
+    const float lse2 = valid ? a.lse2[stat] : INFINITY;
+    const float Dv = valid ? a.D[stat] : 0.f;
+    for (int t = 0; t < inf.cnt; ++t) {
+      const uint32_t e = entries[inf.ebase + t];
+      const uint32_t cls = (e >> 24) & 3u;
+      const int kt = static_cast<int>(e & 0xFFFFFFu);
+      if (!waitw(&bar[B_SFULL], sdp & 1, a, 131)) return;
+      tc_fence_after();
+      float s[64], dp[64];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + tl + half * 64 + 32 * c, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(r[k]);
+        tmem_ld32(tbase + tl + 128 + half * 64 + 32 * c, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dp[32 * c + k] = __uint_as_float(r[k]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[B_SEMPTY]);
+      ++sdp;
+      if (cls == kTilePartial) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t bits = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (!((bits >> k) & 1u)) s[32 * c + k] = -INFINITY;
+        }
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float p0 = ex2_approx(fmaf(s[2 * k], sl2, -lse2));
+        const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, -lse2));
+        pk[k] = pack_bf16x2(p0 * (dp[2 * k] - Dv), p1 * (dp[2 * k + 1] - Dv));
+      }
+      if (dsn >= 1 && !waitw(&bar[B_DSEMPTY], (dsn - 1) & 1, a, 132)) return;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 v = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        *reinterpret_cast<uint4*>(sDS + row * 128 + ((u ^ (row & 7)) << 4)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[B_DSFULL]);
+      ++dsn;
+    }
+    __nv_bfloat16* qrow = dQ + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + inf.head) * kHeadDim +
+                          half * 64;
+    if (inf.cnt > 0) {
+      if (!waitw(&bar[B_DQFULL], items_done & 1, a, 133)) return;
+      ++items_done;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + tl + 256 + half * 64 + 32 * c, r);
+        tmem_ld_wait();
+        if (valid) {
+          float f[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(qrow + 32 * c + 8 * u) = pack8(f + 8 * u, a.scale);
+        }
+      }
+    } else if (valid) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(qrow + 8 * u) = make_uint4(0, 0, 0, 0);
+    }
+    tc_fence_before();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
+  Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
+    mbar_init(&bar[B_SEMPTY], 256);
+    mbar_init(&bar[B_DSFULL], 256);
+    mbar_init(&bar[B_ITEMPTY], 9);
+    mbar_init(&bar[B_ITEMPTY1], 9);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  if (warp == 9) {
+    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
+  } else if (warp == 8) {
+    if (lane == 0) mma_issuer(a, sm, bar, items, tbase);
+  } else {
+    compute(a, sm, bar, items, tbase);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace dq
+
+// ====================================================================== dK / dV
+namespace dkv {
+
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTile128;
+constexpr int kOffQ = kOffV + kTile128;     // 2-slot ring of 64-row Q tiles
+constexpr int kOffDO = kOffQ + 2 * kTile64; // 2-slot ring of 64-row dO tiles
+constexpr int kOffP = kOffDO + 2 * kTile64; // 2 buffers of P^T  [128 keys x 64 queries]
+constexpr int kOffDS = kOffP + 2 * kTile64; // 2 buffers of dS^T
+constexpr int kOffStat = kOffDS + 2 * kTile64;  // 2 buffers of: lse2[64], D[64], mask words[64][4]
+constexpr int kStatBytes = 64 * 4 * 2 + 64 * 4 * 4;
+constexpr int kOffCtl = kOffStat + 2 * kStatBytes;
+constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
+
+enum : int {
+  B_KVFULL = 0, B_KVEMPTY, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_SFULL1, B_SEMPTY, B_SEMPTY1,
+  B_PFULL, B_PFULL1, B_PEMPTY, B_PEMPTY1, B_ACCFULL, B_ITFULL, B_ITFULL1, B_ITEMPTY, B_ITEMPTY1, B_DRAIN, B_STAT,
+  B_COUNT
+};
+
+struct Item {
+  int valid, kg, kt, g, unit_hm, nsteps;  // unit_hm: first map head of the unit's lists
+  int rk, pad;
+};
+
+// Steps of an item: for each query head of the KV head, each entry of its
+// list, each 64-row half of the 128-row query tile that lies inside the
+// segment.  Every role walks them in the same order.
+struct StepIter {
+  const AttnArgs* a;
+  int g, rk;
+  int l, e, half, n_in_list;
+  long long ebase;
+  __device__ void start(const AttnArgs& args, int g_, int kg, int kt, int rk_) {
+    a = &args;
+    g = g_;
+    rk = rk_;
+    l = -1;
+    e = 0;
+    half = 0;
+    n_in_list = 0;
+    (void)kg;
+    (void)kt;
+    next_list();
+  }
+  __device__ void next_list() {
+    const PlanView& pv = a->pv;
+    while (true) {
+      ++l;
+      if (l >= pv.G) return;
+      const int hm = (pv.hm_count == 1) ? 0 : g * pv.G + l;
+      const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
+      const KeyGroup grp = pv.kgs[kg];
+      const int kt = rk - pv.kt_start[kg];
+      n_in_list = a->list_cnt[hm * pv.RK + rk];
+      ebase = hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(kt) * grp.pairs;
+      e = 0;
+      half = 0;
+      if (n_in_list > 0) return;
+    }
+  }
+  // Returns false when done; otherwise the step's segment, head, first query row and class.
+  __device__ bool next(int& seg, int& head, int& r0, uint32_t& cls) {
+    const PlanView& pv = a->pv;
+    const int2* entries = static_cast<const int2*>(a->entries);
+    while (l < pv.G) {
+      if (e >= n_in_list) {
+        next_list();
+        continue;
+      }
+      const int2 en = entries[ebase + e];
+      const int s = en.x;
+      const int qt = en.y & 0xFFFFFF;
+      const int h = half;
+      if (++half == 2) {
+        half = 0;
+        ++e;
+      }
+      const int q_len = pv.segs[s].q_len;
+      const int rr = qt * kTile + 64 * h;
+      if (rr >= q_len) continue;
+      seg = s;
+      head = g * pv.G + l;
+      r0 = rr;
+      cls = static_cast<uint32_t>(en.y >> 24) & 3u;
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ int count_steps(const AttnArgs& a, int g, int rk) {
+  StepIter si;
+  si.start(a, g, 0, 0, rk);
+  int n = 0, s, h, r0;
+  uint32_t c;
+  while (si.next(s, h, r0, c)) ++n;
+  return n;
+}
+
+__device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
+                                         const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
+                                         Item* items) {
+  const PlanView& pv = a.pv;
+  uint32_t steps = 0;
+  int kv_issued = 0;
+  int it = 0;
+  for (;; ++it) {
+    const int slot = it & 1;
+    if (it >= 2 && !wait1(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 210)) goto abort;
+    {
+      const int w = atomicAdd(a.counter, 1);
+      Item inf;
+      inf.valid = 0;
+      if (w < a.n_work) {
+        const int unit = a.order[w / a.expand];
+        const int gm = unit / pv.RK, rk = unit % pv.RK;
+        const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
+        inf.valid = 1;
+        inf.kg = kg;
+        inf.kt = rk - pv.kt_start[kg];
+        inf.rk = rk;
+        inf.g = (pv.hm_count == 1) ? (w % a.expand) : gm;
+        inf.unit_hm = 0;
+        inf.nsteps = count_steps(a, inf.g, rk);
+      }
+      items[slot] = inf;
+      mbar_arrive(&bar[B_ITFULL + slot]);
+      if (!inf.valid) return;
+      const KeyGroup grp = pv.kgs[inf.kg];
+      const int yk = grp.k_off + inf.kt * kTile;
+      if (it >= 1 && !wait1(&bar[B_KVEMPTY], (it - 1) & 1, a, 211)) goto abort;
+      mbar_arrive_expect_tx(&bar[B_KVFULL], 2 * kTile128);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_2d(sm + kOffK + c * kChunk128, tk, &bar[B_KVFULL], inf.g * kHeadDim + c * 64, yk);
+        tma_load_2d(sm + kOffV + c * kChunk128, tv, &bar[B_KVFULL], inf.g * kHeadDim + c * 64, yk);
+      }
+      kv_issued = it + 1;
+      StepIter si;
+      si.start(a, inf.g, inf.kg, inf.kt, inf.rk);
+      int s, h, r0;
+      uint32_t cls;
+      while (si.next(s, h, r0, cls)) {
+        const int b = steps & 1;
+        if (steps >= 2 && !wait1(&bar[B_QEMPTY + b], ((steps >> 1) - 1) & 1, a, 212)) goto abort;
+        mbar_arrive_expect_tx(&bar[B_QFULL + b], 2 * kTile64);
+        const int y = pv.segs[s].q_off + r0;
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(sm + kOffQ + b * kTile64 + c * kChunk64, tq, &bar[B_QFULL + b], h * kHeadDim + c * 64, y);
+          tma_load_2d(sm + kOffDO + b * kTile64 + c * kChunk64, tdo, &bar[B_QFULL + b], h * kHeadDim + c * 64, y);
+        }
+        ++steps;
+      }
+    }
+  }
+abort:
+  for (uint32_t d = 0; d < 2 && d < steps; ++d) {
+    const uint32_t idx = steps - 1 - d;
+    mbar_wait(&bar[B_QFULL + (idx & 1)], (idx >> 1) & 1, nullptr, 100000000ull, 0, 0);
+  }
+  if (kv_issued >= 1) mbar_wait(&bar[B_KVFULL], (kv_issued - 1) & 1, nullptr, 100000000ull, 0, 0);
+}
+
+__device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items,
+                                           uint32_t tbase) {
+  const uint32_t base = smem_u32(sm);
+  const uint32_t k_addr = base + kOffK, v_addr = base + kOffV;
+  uint32_t steps = 0;  // global step counter (rings and TMEM double buffers)
+  int acc_items = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 220)) goto abort;
+    {
+      const Item inf = items[slot];
+      mbar_arrive(&bar[B_ITEMPTY + slot]);
+      if (!inf.valid) return;
+      if (!wait1(&bar[B_KVFULL], it & 1, a, 221)) goto abort;
+      tc_fence_after();
+      const int n = inf.nsteps;
+      for (int p = 0; p <= n; ++p) {
+        if (p < n) {  // S^T = K Q^T, dP^T = V dO^T into TMEM buffer b
+          const uint32_t idx = steps + p;
+          const int b = idx & 1;
+          if (idx >= 2 && !wait1(&bar[B_SEMPTY + b], ((idx >> 1) - 1) & 1, a, 222)) goto abort;
+          if (!wait1(&bar[B_QFULL + b], (idx >> 1) & 1, a, 223)) goto abort;
+          tc_fence_after();
+          const uint32_t q_addr = base + kOffQ + b * kTile64, do_addr = base + kOffDO + b * kTile64;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = (ks >> 2) * kChunk128 + (ks & 3) * 32;
+            const uint32_t bo = (ks >> 2) * kChunk64 + (ks & 3) * 32;
+            umma_ss(tbase + 64 * b, sdesc_sw128(k_addr + ao, 16, 1024), sdesc_sw128(q_addr + bo, 16, 1024), kIdesc64,
+                    ks > 0);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = (ks >> 2) * kChunk128 + (ks & 3) * 32;
+            const uint32_t bo = (ks >> 2) * kChunk64 + (ks & 3) * 32;
+            umma_ss(tbase + 128 + 64 * b, sdesc_sw128(v_addr + ao, 16, 1024), sdesc_sw128(do_addr + bo, 16, 1024),
+                    kIdesc64, ks > 0);
+          }
+          umma_commit(&bar[B_SFULL + b]);
+          if (p == n - 1) umma_commit(&bar[B_KVEMPTY]);
+        }
+        if (p >= 1) {  // dV += P^T dO, dK += dS^T Q for step p-1
+          const uint32_t idx = steps + p - 1;
+          const int b = idx & 1;
+          if (!wait1(&bar[B_PFULL + b], (idx >> 1) & 1, a, 224)) goto abort;
+          tc_fence_after();
+          const uint32_t q_addr = base + kOffQ + b * kTile64, do_addr = base + kOffDO + b * kTile64;
+          const uint32_t p_addr = base + kOffP + b * kTile64, ds_addr = base + kOffDS + b * kTile64;
+          const uint32_t acc = (p > 1) ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            umma_ss(tbase + 256, sdesc_sw128(p_addr + ks * 32, 16, 1024),
+                    sdesc_sw128(do_addr + ks * 2048, kChunk64, 1024), kIdescMN, (ks > 0) ? 1u : acc);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            umma_ss(tbase + 384, sdesc_sw128(ds_addr + ks * 32, 16, 1024),
+                    sdesc_sw128(q_addr + ks * 2048, kChunk64, 1024), kIdescMN, (ks > 0) ? 1u : acc);
+          }
+          umma_commit(&bar[B_PEMPTY + b]);
+          umma_commit(&bar[B_QEMPTY + b]);
+          if (p == n) umma_commit(&bar[B_ACCFULL]);
+        }
+      }
+      if (n == 0) umma_commit(&bar[B_KVEMPTY]);
+      steps += n;
+      acc_items += (n > 0);
+    }
+  }
+abort:
+  umma_commit(&bar[B_DRAIN]);
+  mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
+}
+
+__device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
+  const PlanView& pv = a.pv;
+  const int warp = threadIdx.x >> 5;
+  const int wq = warp & 3, half = warp >> 2;  // half: which 32 of the 64 query columns
+  const int lane = threadIdx.x & 31;
+  const int j = wq * 32 + lane;  // key row inside the tile = TMEM lane
+  const int ctid = threadIdx.x;  // 0..255
+  const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
+  const float sl2 = a.scale_log2;
+  __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(a.dk);
+  __nv_bfloat16* dV = static_cast<__nv_bfloat16*>(a.dv);
+  uint32_t steps = 0, acc_items = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 230)) return;
+    const Item inf = items[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
+    if (!inf.valid) return;
+    const KeyGroup grp = pv.kgs[inf.kg];
+    StepIter si;
+    si.start(a, inf.g, inf.kg, inf.kt, inf.rk);
+    int s, h, r0;
+    uint32_t cls;
+    while (si.next(s, h, r0, cls)) {
+      const SegInfo sg = pv.segs[s];
+      const int b = steps & 1;
+      // Stage this step's per-query statistics and, on partial tiles, the mask
+      // words in buffer b; the buffer of step p+2 is written only after every
+      // thread has passed the staging barrier of step p+1, hence done with p.
+      float* s_lse2 = reinterpret_cast<float*>(sm + kOffStat + b * kStatBytes);
+      float* s_D = s_lse2 + 64;
+      uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_D + 64);  // [64 query rows][4 key chunks]
+      if (ctid < 64) {
+        const int i = r0 + ctid;
+        const size_t st = static_cast<size_t>(h) * pv.Tq + sg.q_off + i;
+        const bool ok = i < sg.q_len;
+        s_lse2[ctid] = ok ? a.lse2[st] : INFINITY;
+        s_D[ctid] = ok ? a.D[st] : 0.f;
+      }
+      if (cls == kTilePartial) {
+        const int qi = ctid >> 2, c = ctid & 3;
+        const int hm = (pv.hm_count == 1) ? 0 : h;
+        s_mask[ctid] = mask_bits(pv.mask, sg, hm, r0 + qi, inf.kt * kTile + 32 * c);
+      }
+      mbar_arrive(&bar[B_STAT]);
+      if (!waitw(&bar[B_STAT], steps & 1, a, 234)) return;
+      if (!waitw(&bar[B_SFULL + b], (steps >> 1) & 1, a, 231)) return;
+      tc_fence_after();
+      float sv[32], dp[32];
+      {
+        uint32_t r[32];
+        tmem_ld32(tbase + tl + 64 * b + 32 * half, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) sv[k] = __uint_as_float(r[k]);
+        tmem_ld32(tbase + tl + 128 + 64 * b + 32 * half, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[B_SEMPTY + b]);
+      if (cls == kTilePartial) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const uint32_t w = s_mask[(32 * half + k) * 4 + wq];
+          if (!((w >> lane) & 1u)) sv[k] = -INFINITY;
+        }
+      }
+      uint32_t pp[16], pd[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int q0 = 32 * half + 2 * k;
+        const float p0 = ex2_approx(fmaf(sv[2 * k], sl2, -s_lse2[q0]));
+        const float p1 = ex2_approx(fmaf(sv[2 * k + 1], sl2, -s_lse2[q0 + 1]));
+        pp[k] = pack_bf16x2(p0, p1);
+        pd[k] = pack_bf16x2(p0 * (dp[2 * k] - s_D[q0]), p1 * (dp[2 * k + 1] - s_D[q0 + 1]));
+      }
+      if (steps >= 2 && !waitw(&bar[B_PEMPTY + b], ((steps >> 1) - 1) & 1, a, 232)) return;
+      // P^T and dS^T rows: [128 keys x 64 queries], K-major, one 128-byte swizzle chunk;
+      // this thread writes the 4 x 16-byte pieces of its 32 query columns.
+      uint8_t* pbuf = sm + kOffP + b * kTile64;
+      uint8_t* dbuf = sm + kOffDS + b * kTile64;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int piece = 4 * half + u;
+        const uint32_t off = j * 128 + ((piece ^ (j & 7)) << 4);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
+        *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bar[B_PFULL + b]);
+      ++steps;
+    }
+    // epilogue: rows of the key group only
+    const int jg = inf.kt * kTile + j;
+    const bool valid = jg < grp.k_len;
+    const size_t orow = (static_cast<size_t>(grp.k_off + (valid ? jg : 0)) * pv.Hkv + inf.g) * kHeadDim + half * 64;
+    if (inf.nsteps > 0) {
+      if (!waitw(&bar[B_ACCFULL], acc_items & 1, a, 233)) return;
+      ++acc_items;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        float f[32];
+        tmem_ld32(tbase + tl + 256 + half * 64 + 32 * c, r);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dV + orow + 32 * c + 8 * u) = pack8(f + 8 * u, 1.f);
+        }
+        tmem_ld32(tbase + tl + 384 + half * 64 + 32 * c, r);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            *reinterpret_cast<uint4*>(dK + orow + 32 * c + 8 * u) = pack8(f + 8 * u, a.scale);
+        }
+      }
+    } else if (valid) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        *reinterpret_cast<uint4*>(dV + orow + 8 * u) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(dK + orow + 8 * u) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    tc_fence_before();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
+  Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
+    mbar_init(&bar[B_SEMPTY], 256);
+    mbar_init(&bar[B_SEMPTY1], 256);
+    mbar_init(&bar[B_PFULL], 256);
+    mbar_init(&bar[B_PFULL1], 256);
+    mbar_init(&bar[B_STAT], 256);
+    mbar_init(&bar[B_ITEMPTY], 9);
+    mbar_init(&bar[B_ITEMPTY1], 9);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  if (warp == 9) {
+    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
+  } else if (warp == 8) {
+    if (lane == 0) mma_issuer(a, sm, bar, items, tbase);
+  } else {
+    compute(a, sm, bar, items, tbase);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace dkv
+}  // namespace
+
+void launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                   const AttnArgs& a, int num_sms, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(dq::dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    configured = true;
+  }
+  const int grid = max(1, min(num_sms, a.n_work));
+  note_launches(1);
+  dq::dq_kernel<<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+}
+
+void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                    const AttnArgs& a, int num_sms, cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(dkv::dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    configured = true;
+  }
+  const int grid = max(1, min(num_sms, a.n_work));
+  note_launches(1);
+  dkv::dkv_kernel<<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+}
+
+}  // namespace lca

@@ -1,0 +1,277 @@
+// lca_common.cuh — structures shared by the host planner and the kernels, and
+// the one device mask predicate that every kernel (materializer, tile
+// classifier, forward, backward) evaluates.
+//
+// The mask families are the ones the LongCA-bench review lists (三 技术架构,
+// 掩码模式分类); the page names them without formulas, so each family is
+// encoded here by the plainest reading (see the lca_mask_kind comments in
+// lca_attn.h).  For every family except the block-sparse ones, the keys a
+// query row attends form at most two intervals of the segment's key axis;
+// the kernels turn those into 32-column bit masks only on partially masked
+// tiles.
+#pragma once
+#include <cstdint>
+
+namespace lca {
+
+constexpr int kTile = 128;  // query and key tile edge
+constexpr int kHeadDim = 128;
+
+enum MaskKind : int {
+  kFull = 0,
+  kCausal = 1,
+  kSliding = 2,
+  kCausalSliding = 3,
+  kDoc = 4,
+  kCausalDoc = 5,
+  kSharedQuestion = 6,
+  kGlobalSliding = 7,
+  kCausalBlockwise = 8,
+  kPrefixLmCausal = 9,
+  kPrefixLmDoc = 10,
+  kBlockCausalDoc = 11,
+  kBlockSparseUniform = 12,
+  kBlockSparseVariable = 13,
+};
+
+enum TileClass : uint32_t { kTileEmpty = 0, kTileFull = 1, kTilePartial = 2 };
+
+// Status codes written to the device status word (mirror lca_status).
+constexpr int kStatusTimeout = 5;
+constexpr int kStatusDeviceArg = 6;
+
+struct SegInfo {  // 32 bytes
+  int q_off, q_len, k_off, k_len;
+  int prefix;  // PREFIX_LM_DOC prefix of this segment
+  int kg;      // key group index
+  int nk;      // number of 128-key tiles = ceil(k_len / 128)
+  int pad;
+};
+
+struct KeyGroup {  // 32 bytes
+  int k_off, k_len;        // k_len = longest member's k_len
+  int seg_begin, seg_end;  // members: kg_segs[seg_begin, seg_end)
+  int kt_start;            // first dK/dV unit row of this group
+  int pairs;               // sum of members' 128-row query tiles
+  long long entry_off;     // offset of this group's dK/dV entries (per map head)
+};
+
+struct MaskCtx {
+  int kind;
+  int wl, wr, ng, prefix, block;
+  int n_parts;       // number of part bounds (SHARED_QUESTION)
+  const int* parts;  // device copy of the part bounds
+  // block-sparse
+  int q_block, kv_block;
+  int n_qb, n_kb, words;  // words = ceil(n_kb / 32)
+  int hm_count;           // heads_in_map (1 or Hq)
+  const uint32_t* keep;   // [hm][n_qb][words] bitmap built from the CSR
+  const int* qb_of;       // variable: query block of each global row [Tq]
+  const int* kb_of;       // variable: key block of each global key [Tk]
+  const int* kb_start;    // variable: key block bounds [n_kb + 1]
+  const int* qb_start;    // variable: query block bounds [n_qb + 1]
+};
+
+__host__ __device__ __forceinline__ bool is_block_sparse(int kind) {
+  return kind == kBlockSparseUniform || kind == kBlockSparseVariable;
+}
+
+// Largest s in [0, n) with start[s] <= x (start non-decreasing, start[0] = 0).
+__device__ __forceinline__ int find_bucket(const int* __restrict__ start, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (start[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ int floordiv_i(int a, int b) { return (a >= 0) ? a / b : -((-a + b - 1) / b); }
+
+// Keys attended by one query row, as [a0, b0) U [a1, b1), segment-relative,
+// clipped to [0, k_len).  Rows outside [0, q_len) attend nothing.
+struct Span {
+  int a0, b0, a1, b1;
+};
+
+__device__ __forceinline__ Span row_span(const MaskCtx& m, const SegInfo& sg, int i) {
+  Span s{0, 0, 0, 0};
+  if (i < 0 || i >= sg.q_len) return s;
+  const int K = sg.k_len;
+  const int ie = i + (sg.k_len - sg.q_len);  // bottom-right aligned query position
+  switch (m.kind) {
+    case kFull:
+    case kDoc:
+      s.b0 = K;
+      break;
+    case kCausal:
+    case kCausalDoc:
+      s.b0 = ie + 1;
+      break;
+    case kSliding:
+      s.a0 = ie - m.wl;
+      s.b0 = ie + m.wr + 1;
+      break;
+    case kCausalSliding:
+      s.a0 = ie - m.wl;
+      s.b0 = ie + 1;
+      break;
+    case kSharedQuestion: {
+      if (ie < 0) break;
+      int p = 0;  // part holding position ie: largest p with parts[p] <= ie
+      for (int t = 1; t < m.n_parts; ++t) p = (m.parts[t] <= ie) ? t : p;
+      if (p == 0) {
+        s.b0 = ie + 1;
+      } else {
+        s.b0 = m.parts[1];
+        s.a1 = m.parts[p];
+        s.b1 = ie + 1;
+      }
+      break;
+    }
+    case kGlobalSliding:
+      if (ie < m.ng) {
+        s.b0 = K;
+      } else {
+        s.b0 = m.ng;
+        s.a1 = ie - m.wl;
+        s.b1 = ie + m.wr + 1;
+      }
+      break;
+    case kCausalBlockwise: {
+      if (ie < 0) break;
+      const int blk = ie / m.block, last = (K - 1) / m.block;
+      s.a0 = (blk == last) ? 0 : blk * m.block;
+      s.b0 = ie + 1;
+      break;
+    }
+    case kPrefixLmCausal:
+      s.b0 = max(m.prefix, ie + 1);
+      break;
+    case kPrefixLmDoc:
+      s.b0 = max(sg.prefix, ie + 1);
+      break;
+    case kBlockCausalDoc:
+      s.b0 = (floordiv_i(ie, m.block) + 1) * m.block;
+      break;
+    default:
+      break;
+  }
+  s.a0 = max(s.a0, 0);
+  s.b0 = min(s.b0, K);
+  s.a1 = max(s.a1, 0);
+  s.b1 = min(s.b1, K);
+  return s;
+}
+
+// Bits of [a, b) inside the 32 columns [j0, j0 + 32).
+__device__ __forceinline__ uint32_t range_bits(int a, int b, int j0) {
+  const int lo = max(a - j0, 0), hi = min(b - j0, 32);
+  if (hi <= lo) return 0u;
+  const uint32_t upper = (hi >= 32) ? 0xFFFFFFFFu : ((1u << hi) - 1u);
+  const uint32_t lower = (1u << lo) - 1u;
+  return upper & ~lower;
+}
+
+__device__ __forceinline__ uint32_t span_bits(const Span& s, int j0) {
+  return range_bits(s.a0, s.b0, j0) | range_bits(s.a1, s.b1, j0);
+}
+
+__device__ __forceinline__ bool span_covers(const Span& s, int c0, int c1) {
+  const bool e0 = s.a0 < s.b0, e1 = s.a1 < s.b1;
+  if (e0 && s.a0 <= c0 && s.b0 >= c1) return true;
+  if (e1 && s.a1 <= c0 && s.b1 >= c1) return true;
+  if (e0 && e1 && s.a1 <= s.b0 && s.a0 <= s.b1) {
+    const int lo = min(s.a0, s.a1), hi = max(s.b0, s.b1);
+    if (lo <= c0 && hi >= c1) return true;
+  }
+  return false;
+}
+
+__device__ __forceinline__ bool span_hits(const Span& s, int c0, int c1) {
+  return (s.a0 < s.b0 && s.a0 < c1 && s.b0 > c0) || (s.a1 < s.b1 && s.a1 < c1 && s.b1 > c0);
+}
+
+__device__ __forceinline__ int span_count(const Span& s) {
+  const int n0 = max(0, s.b0 - s.a0), n1 = max(0, s.b1 - s.a1);
+  const int lo = max(s.a0, s.a1), hi = min(s.b0, s.b1);
+  const int both = (n0 > 0 && n1 > 0) ? max(0, hi - lo) : 0;
+  return n0 + n1 - both;
+}
+
+// ---------------------------------------------------------------- block-sparse
+__device__ __forceinline__ int q_block_of(const MaskCtx& m, int gq) {
+  return (m.kind == kBlockSparseUniform) ? gq / m.q_block : m.qb_of[gq];
+}
+__device__ __forceinline__ int k_block_of(const MaskCtx& m, int gk) {
+  return (m.kind == kBlockSparseUniform) ? gk / m.kv_block : m.kb_of[gk];
+}
+__device__ __forceinline__ int k_block_start(const MaskCtx& m, int kb) {
+  return (m.kind == kBlockSparseUniform) ? kb * m.kv_block : m.kb_start[kb];
+}
+__device__ __forceinline__ bool block_kept(const MaskCtx& m, int hm, int qb, int kb) {
+  const uint32_t w = m.keep[(static_cast<size_t>(hm) * m.n_qb + qb) * m.words + (kb >> 5)];
+  return (w >> (kb & 31)) & 1u;
+}
+
+// 32-column mask chunk for block-sparse maps.  A chunk touches at most two
+// key blocks because every key block but the last is at least 32 wide.
+__device__ __forceinline__ uint32_t block_chunk_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
+  if (i < 0 || i >= sg.q_len || j0 >= sg.k_len) return 0u;
+  const int qb = q_block_of(m, sg.q_off + i);
+  const int jl = min(j0 + 31, sg.k_len - 1);
+  const int gj0 = sg.k_off + j0;
+  const int kA = k_block_of(m, gj0), kB = k_block_of(m, sg.k_off + jl);
+  const bool keepA = block_kept(m, hm, qb, kA);
+  uint32_t bits;
+  if (kA == kB) {
+    bits = keepA ? 0xFFFFFFFFu : 0u;
+  } else {
+    const bool keepB = block_kept(m, hm, qb, kB);
+    const int split = k_block_start(m, kB) - gj0;  // 1..31
+    const uint32_t low = (1u << split) - 1u;
+    bits = (keepA ? low : 0u) | (keepB ? ~low : 0u);
+  }
+  return bits & range_bits(0, sg.k_len, j0);
+}
+
+// The mask predicate: bit t of the result is set iff query row i of the
+// segment attends key j0 + t (segment-relative), for query head map index hm.
+__device__ __forceinline__ uint32_t mask_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
+  if (is_block_sparse(m.kind)) return block_chunk_bits(m, sg, hm, i, j0);
+  return span_bits(row_span(m, sg, i), j0);
+}
+
+// Class of the 128x128 tile with rows [r0, r0+128) and keys [c0, c0+128) of
+// one segment: EMPTY if no valid cell is attended, FULL if the tile lies
+// inside the segment and every cell is attended, PARTIAL otherwise.  All 32
+// lanes of the warp must call it; every lane gets the result.
+__device__ __forceinline__ uint32_t classify_tile_warp(const MaskCtx& m, const SegInfo& sg, int hm, int r0, int c0) {
+  const int lane = threadIdx.x & 31;
+  const int r1 = min(r0 + kTile, sg.q_len), c1 = min(c0 + kTile, sg.k_len);
+  if (r1 <= r0 || c1 <= c0) return kTileEmpty;
+  const bool inside = (r0 + kTile <= sg.q_len) && (c0 + kTile <= sg.k_len);
+  bool any = false, all = true;
+  if (is_block_sparse(m.kind)) {
+    const int qbA = q_block_of(m, sg.q_off + r0), qbB = q_block_of(m, sg.q_off + r1 - 1);
+    const int kbA = k_block_of(m, sg.k_off + c0), kbB = k_block_of(m, sg.k_off + c1 - 1);
+    const int nq = qbB - qbA + 1, nk = kbB - kbA + 1;
+    for (int t = lane; t < nq * nk; t += 32) {
+      const bool kept = block_kept(m, hm, qbA + t / nk, kbA + t % nk);
+      any |= kept;
+      all &= kept;
+    }
+  } else {
+    for (int r = r0 + lane; r < r1; r += 32) {
+      const Span s = row_span(m, sg, r);
+      any |= span_hits(s, c0, c1);
+      all &= span_covers(s, c0, c1);
+    }
+  }
+  any = __any_sync(0xFFFFFFFFu, any);
+  all = __all_sync(0xFFFFFFFFu, all);
+  if (!any) return kTileEmpty;
+  return (all && inside) ? kTileFull : kTilePartial;
+}
+
+}  // namespace lca

@@ -1,0 +1,467 @@
+// lca_fwd.cu — masked attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// What it computes, per query row i of a segment and query head h:
+//   O_i = sum_j P_ij V_j,  P_ij = exp(tau q_i.k_j - LSE_i) over attended keys,
+//   LSE_i = log sum_j exp(tau q_i.k_j)   (natural log, -inf for no key).
+// How (FlashAttention review page, FlashAttention-1 核心优化 and
+// FlashAttention-2 核心优化): tiles of Q, K, V are staged in shared memory,
+// scores live only on chip, the softmax is computed online with a running
+// max and sum, the output is rescaled lazily and normalised once, and one
+// statistic (LSE) per row is written.  Work is split over query blocks
+// (Q-split), and the elementwise mask is applied only on tiles the mask
+// compiler classified PARTIAL.
+//
+// GB300 mapping.  One persistent CTA per SM, 10 warps:
+//   warp 9       TMA producer: claims work items from the cost-sorted list
+//                through an atomic counter, loads Q (two 128-row sub-tiles)
+//                and streams K/V tiles through a 3-stage ring;
+//   warp 8       MMA issuer: S_x = Q_x K^T and O_x += P_x V with tcgen05.mma,
+//                accumulators in TMEM (S0, S1, O0, O1: 4 x 128 columns);
+//   warps 0-7    two softmax warpgroups, one per 128-row sub-tile; thread r
+//                owns TMEM lane r (row r): it reads the score row, applies
+//                the mask, runs the online softmax in base 2, rescales O in
+//                TMEM only when its running max grows by more than 2^8,
+//                writes P (bf16) to shared memory, and at the end normalises
+//                O and writes O and LSE.
+// While one warpgroup computes exponentials the tensor core runs the other
+// sub-tile's products.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "lca_internal.h"
+#include "sm103.cuh"
+
+namespace lca {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 3;
+constexpr uint32_t kTileBytes = 32768;   // 128 rows x 128 bf16
+constexpr uint32_t kChunkBytes = 16384;  // 128 rows x 64 bf16: one 128-byte-swizzled TMA box
+constexpr int kOffQ = 0;                 // Q sub-tile x at x * kTileBytes
+constexpr int kOffKV = 2 * kTileBytes;   // K/V ring
+constexpr int kOffP = kOffKV + kStages * kTileBytes;  // P sub-tile x at + x * kTileBytes
+constexpr int kOffCtl = kOffP + 2 * kTileBytes;
+constexpr int kSmemBytes = kOffCtl + 1024 + 1024;  // control block + alignment slack
+
+enum : int {
+  B_QFULL = 0,
+  B_QEMPTY = 1,
+  B_KVFULL = 2,
+  B_KVEMPTY = B_KVFULL + kStages,
+  B_SFULL = B_KVEMPTY + kStages,
+  B_SEMPTY = B_SFULL + 2,
+  B_PFULL = B_SEMPTY + 2,
+  B_OFULL = B_PFULL + 2,
+  B_ITFULL = B_OFULL + 2,
+  B_ITEMPTY = B_ITFULL + 2,
+  B_DRAIN = B_ITEMPTY + 2,
+  B_COUNT = B_DRAIN + 1
+};
+
+struct Item {  // 32 bytes, broadcast from the producer to the other roles
+  int valid, seg, qb, head, hm, cnt;
+  long long ebase;
+};
+
+constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T (both K-major)
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);   // O += P V (V is N-major)
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// Ring position of the u-th load of an item with n tiles: loads follow the
+// order the MMA warp consumes them: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1).
+__device__ __forceinline__ uint32_t k_load_index(int t) { return t == 0 ? 0u : static_cast<uint32_t>(2 * t - 1); }
+__device__ __forceinline__ uint32_t v_load_index(int t, int n) {
+  return (t == n - 1) ? static_cast<uint32_t>(2 * n - 1) : static_cast<uint32_t>(2 * t + 2);
+}
+
+__device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const AttnArgs& a, int where) {
+  return mbar_wait(bar, parity, a.status, a.wait_limit_ns, kStatusTimeout, where);
+}
+// Warp-uniform wait: every lane polls, the warp proceeds only if all succeed.
+__device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, const AttnArgs& a, int where) {
+  const bool ok = mbar_wait(bar, parity, a.status, a.wait_limit_ns, kStatusTimeout, where);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// ------------------------------------------------------------------ producer
+__device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
+                                         const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, uint64_t* bar,
+                                         Item* items) {
+  const PlanView& pv = a.pv;
+  const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  uint32_t kv_iter = 0;
+  uint32_t issued = 0;  // K/V loads issued (ring index of the next one)
+  int q_issued = 0;     // Q loads issued
+  int it = 0;
+  for (;; ++it) {
+    const int slot = it & 1;
+    if (it >= 2 && !wait1(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 10)) goto abort;
+    {
+      const int w = atomicAdd(a.counter, 1);
+      Item inf;
+      inf.valid = 0;
+      if (w < a.n_work) {
+        const int row = a.order[w / a.expand];
+        const int hm = row / pv.R256, rr = row % pv.R256;
+        const int s = find_bucket(pv.q256_start, pv.n_seg, rr);
+        inf.valid = 1;
+        inf.seg = s;
+        inf.qb = rr - pv.q256_start[s];
+        inf.hm = hm;
+        inf.head = (pv.hm_count == 1) ? (w % a.expand) : hm;
+        inf.cnt = a.cnt[row];
+        inf.ebase = hm * pv.fwd_per_hm + pv.fwd_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk;
+      }
+      items[slot] = inf;
+      mbar_arrive(&bar[B_ITFULL + slot]);
+      if (!inf.valid) return;
+
+      const SegInfo sg = pv.segs[inf.seg];
+      if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 11)) goto abort;
+      mbar_arrive_expect_tx(&bar[B_QFULL], 2 * kTileBytes);
+      const int y0 = sg.q_off + inf.qb * 2 * kTile;
+#pragma unroll
+      for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_2d(sQ + x * kTileBytes + c * kChunkBytes, tq, &bar[B_QFULL], inf.head * kHeadDim + c * 64,
+                      y0 + x * kTile);
+      q_issued = it + 1;
+
+      const int g = inf.head / pv.G;
+      const int n = inf.cnt;
+      for (int u = 0; u < 2 * n; ++u) {
+        int t;
+        bool is_v;
+        if (u == 0) { t = 0; is_v = false; }
+        else if (u & 1) {
+          t = (u + 1) >> 1;
+          is_v = (t >= n);
+          if (is_v) t = n - 1;
+        } else { t = (u >> 1) - 1; is_v = true; }
+        const int kt = static_cast<int>(entries[inf.ebase + t] & 0xFFFFFFu);
+        const uint32_t idx = kv_iter + u;
+        const int stg = idx % kStages;
+        if (idx >= kStages && !wait1(&bar[B_KVEMPTY + stg], ((idx / kStages) - 1) & 1, a, 12)) goto abort;
+        mbar_arrive_expect_tx(&bar[B_KVFULL + stg], kTileBytes);
+        const CUtensorMap* m = is_v ? tv : tk;
+        const int yk = sg.k_off + kt * kTile;
+        tma_load_2d(sKV + stg * kTileBytes, m, &bar[B_KVFULL + stg], g * kHeadDim, yk);
+        tma_load_2d(sKV + stg * kTileBytes + kChunkBytes, m, &bar[B_KVFULL + stg], g * kHeadDim + 64, yk);
+        issued = idx + 1;
+      }
+      kv_iter += 2 * n;
+    }
+  }
+abort:
+  // Let the copies already issued land before the CTA leaves.
+  for (uint32_t d = 0; d < kStages && d < issued; ++d) {
+    const uint32_t idx = issued - 1 - d;
+    mbar_wait(&bar[B_KVFULL + idx % kStages], (idx / kStages) & 1, nullptr, 100000000ull, 0, 0);
+  }
+  if (q_issued >= 1) mbar_wait(&bar[B_QFULL], (q_issued - 1) & 1, nullptr, 100000000ull, 0, 0);
+}
+
+// ------------------------------------------------------------------ MMA issuer
+__device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8_t* sKV, uint8_t* sP, uint64_t* bar,
+                                           Item* items, uint32_t tbase) {
+  const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  const uint32_t q_addr = smem_u32(sQ), kv_addr = smem_u32(sKV), p_addr = smem_u32(sP);
+  uint32_t kv_iter = 0;
+  uint32_t s_iss[2] = {0, 0}, p_iss[2] = {0, 0};
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 20)) goto abort;
+    {
+      const Item inf = items[slot];
+      mbar_arrive(&bar[B_ITEMPTY + slot]);
+      if (!inf.valid) return;
+      if (!wait1(&bar[B_QFULL], it & 1, a, 21)) goto abort;
+      tc_fence_after();
+      const int n = inf.cnt;
+      bool first_pv[2] = {true, true};
+      for (int t = 0; t <= n; ++t) {
+        if (t < n) {  // S_x(t) = Q_x K(t)^T
+          const uint32_t e = entries[inf.ebase + t];
+          const uint32_t idx = kv_iter + k_load_index(t);
+          const int stg = idx % kStages;
+          if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 22)) goto abort;
+          tc_fence_after();
+          const uint32_t k_addr = kv_addr + stg * kTileBytes;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (((e >> (24 + 2 * x)) & 3u) == 0) continue;
+            if (s_iss[x] >= 1 && !wait1(&bar[B_SEMPTY + x], (s_iss[x] - 1) & 1, a, 23)) goto abort;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t koff = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
+              umma_ss(tbase + 128 * x, sdesc_sw128(q_addr + x * kTileBytes + koff, 16, 1024),
+                      sdesc_sw128(k_addr + koff, 16, 1024), kIdescS, ks > 0 ? 1u : 0u);
+            }
+            umma_commit(&bar[B_SFULL + x]);
+            ++s_iss[x];
+          }
+          umma_commit(&bar[B_KVEMPTY + stg]);
+          if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
+        }
+        if (t >= 1) {  // O_x += P_x(t-1) V(t-1)
+          const int u = t - 1;
+          const uint32_t e = entries[inf.ebase + u];
+          const uint32_t idx = kv_iter + v_load_index(u, n);
+          const int stg = idx % kStages;
+          if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 24)) goto abort;
+          tc_fence_after();
+          const uint32_t v_addr = kv_addr + stg * kTileBytes;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (((e >> (24 + 2 * x)) & 3u) == 0) continue;
+            if (!wait1(&bar[B_PFULL + x], p_iss[x] & 1, a, 25)) goto abort;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t poff = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
+              umma_ss(tbase + 256 + 128 * x, sdesc_sw128(p_addr + x * kTileBytes + poff, 16, 1024),
+                      sdesc_sw128(v_addr + ks * 2048, kChunkBytes, 1024), kIdescO,
+                      (ks > 0 || !first_pv[x]) ? 1u : 0u);
+            }
+            first_pv[x] = false;
+            umma_commit(&bar[B_OFULL + x]);
+            ++p_iss[x];
+          }
+          umma_commit(&bar[B_KVEMPTY + stg]);
+        }
+      }
+      if (n == 0) umma_commit(&bar[B_QEMPTY]);
+      kv_iter += 2 * n;
+    }
+  }
+abort:
+  umma_commit(&bar[B_DRAIN]);
+  mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
+}
+
+// ------------------------------------------------------------------ softmax warpgroup
+__device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP, uint64_t* bar, Item* items,
+                                           uint32_t tbase) {
+  const PlanView& pv = a.pv;
+  const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  const int wq = (threadIdx.x >> 5) & 3;
+  const int lane = threadIdx.x & 31;
+  const int row = wq * 32 + lane;  // TMEM lane = row of the sub-tile
+  const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tbase + tl + 128 * x;
+  const uint32_t tO = tbase + tl + 256 + 128 * x;
+  uint8_t* myP = sP + x * kTileBytes;
+  __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o);
+  const float sl2 = a.scale_log2;
+  uint32_t s_cons = 0, p_prod = 0;
+  for (int it = 0;; ++it) {
+    const int slot = it & 1;
+    if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 30 + x)) return;
+    const Item inf = items[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
+    if (!inf.valid) return;
+    const SegInfo sg = pv.segs[inf.seg];
+    const int i = inf.qb * 2 * kTile + x * kTile + row;  // row inside the segment
+    const bool valid = i < sg.q_len;
+    float m_use = -INFINITY, l = 0.f;
+    bool any = false;
+    for (int t = 0; t < inf.cnt; ++t) {
+      const uint32_t e = entries[inf.ebase + t];
+      const uint32_t cls = (e >> (24 + 2 * x)) & 3u;
+      if (cls == kTileEmpty) continue;
+      const int kt = static_cast<int>(e & 0xFFFFFFu);
+      if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tS + 32 * c, r);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(r[k]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[B_SEMPTY + x]);
+      ++s_cons;
+      if (cls == kTilePartial) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t bits = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (!((bits >> k) & 1u)) s[32 * c + k] = -INFINITY;
+        }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      const float m_new = fmaxf(m_use, mx * sl2);
+      float factor = 1.f;
+      bool need = false;
+      if (!any) {
+        m_use = m_new;
+      } else if (m_new > m_use + kRescaleThreshold) {
+        factor = ex2_approx(m_use - m_new);
+        need = true;
+        m_use = m_new;
+      }
+      const float base = (m_use == -INFINITY) ? 0.f : m_use;
+      float sum = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int k = 0; k < 64; ++k) {
+        const float p0 = ex2_approx(fmaf(s[2 * k], sl2, -base));
+        const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, -base));
+        sum += p0 + p1;
+        pk[k] = pack_bf16x2(p0, p1);
+      }
+      l = l * factor + sum;
+      if (any) {
+        // the previous O_x += P_x V has finished: P_x may be overwritten and O_x is stable
+        if (!waitw(&bar[B_OFULL + x], (p_prod - 1) & 1, a, 34 + x)) return;
+        tc_fence_after();
+      }
+      if (__any_sync(0xFFFFFFFFu, need)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tO + 32 * c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * factor);
+          tmem_st32(tO + 32 * c, r);
+        }
+        tmem_st_wait();
+      }
+      // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = make_uint4(pk[32 * kc + 4 * u], pk[32 * kc + 4 * u + 1], pk[32 * kc + 4 * u + 2],
+                                     pk[32 * kc + 4 * u + 3]);
+          *reinterpret_cast<uint4*>(myP + kc * kChunkBytes + row * 128 + ((u ^ (row & 7)) << 4)) = v;
+        }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bar[B_PFULL + x]);
+      ++p_prod;
+      any = true;
+    }
+    // epilogue: O = O / l (bf16), LSE = (m + log2 l) ln 2
+    __nv_bfloat16* orow = O + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + inf.head) * kHeadDim;
+    if (any) {
+      if (!waitw(&bar[B_OFULL + x], (p_prod - 1) & 1, a, 36 + x)) return;
+      tc_fence_after();
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tO + 32 * c, r);
+        tmem_ld_wait();
+        if (valid) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv, __uint_as_float(r[8 * u + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv, __uint_as_float(r[8 * u + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv, __uint_as_float(r[8 * u + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv, __uint_as_float(r[8 * u + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) = v;
+          }
+        }
+      }
+    } else if (valid) {
+#pragma unroll
+      for (int u = 0; u < 16; ++u) *reinterpret_cast<uint4*>(orow + 8 * u) = make_uint4(0, 0, 0, 0);
+    }
+    if (valid) {
+      a.lse[static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i] =
+          (l > 0.f) ? (m_use + log2f(l)) * kLn2 : -INFINITY;
+    }
+    tc_fence_before();
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm + kOffQ;
+  uint8_t* sKV = sm + kOffKV;
+  uint8_t* sP = sm + kOffP;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
+  Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 8) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[B_QFULL], 1);
+    mbar_init(&bar[B_QEMPTY], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar[B_KVFULL + s], 1);
+      mbar_init(&bar[B_KVEMPTY + s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bar[B_SFULL + x], 1);
+      mbar_init(&bar[B_SEMPTY + x], 128);
+      mbar_init(&bar[B_PFULL + x], 128);
+      mbar_init(&bar[B_OFULL + x], 1);
+      mbar_init(&bar[B_ITFULL + x], 1);
+      mbar_init(&bar[B_ITEMPTY + x], 9);
+    }
+    mbar_init(&bar[B_DRAIN], 1);
+    fence_mbar_init();
+  }
+  if (warp == 9 && lane == 0) {
+    tma_prefetch_map(&tmQ);
+    tma_prefetch_map(&tmK);
+    tma_prefetch_map(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 9) {
+    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, sQ, sKV, bar, items);
+  } else if (warp == 8) {
+    if (lane == 0) mma_issuer(a, sQ, sKV, sP, bar, items, tbase);
+  } else {
+    softmax_wg(a, warp >> 2, sP, bar, items, tbase);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace
+
+void launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a, int num_sms,
+                cudaStream_t st) {
+  static bool configured = false;
+  if (!configured) {
+    cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    configured = true;
+  }
+  const int grid = max(1, min(num_sms, a.n_work));
+  note_launches(1);
+  fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+}
+
+}  // namespace lca

@@ -1,0 +1,94 @@
+// lca_internal.h — what the host side (lca_api.cu) and the kernel files share:
+// the device view of a call's plan and the kernel launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "lca_common.cuh"
+
+namespace lca {
+
+constexpr int kCostBuckets = 4096;  // histogram buckets of the cost sort
+
+// Counts kernel launches made by this library (see lca_launch_count).
+void note_launches(int n);
+
+// Device-side view of one call's plan; every pointer lies in the workspace.
+struct PlanView {
+  MaskCtx mask;
+  const SegInfo* segs;
+  int n_seg;
+  const int* q256_start;     // [n_seg + 1] prefix of 256-row query blocks
+  const int* q128_start;     // [n_seg + 1] prefix of 128-row query tiles
+  const long long* fwd_off;  // [n_seg] forward entry offset of each segment (per map head)
+  const long long* dq_off;   // [n_seg] dQ entry offset of each segment (per map head)
+  const KeyGroup* kgs;
+  int n_kg;
+  const int* kg_segs;   // segment ids grouped by key group
+  const int* kt_start;  // [n_kg + 1] prefix of key tiles
+  int hm_count;         // mask map heads H' (1 or Hq)
+  int R256, R128, RK;   // rows per map head: 256-row blocks, 128-row tiles, key tiles
+  long long fwd_per_hm, dq_per_hm, dkv_per_hm;
+  int Tq, Tk, Hq, Hkv, G;
+};
+
+// Work lists produced by the planner for one kernel.
+struct WorkList {
+  int* cnt;           // entries per list row
+  int* order;         // rows (or units) sorted by descending cost
+  void* entries;      // uint32 (query-major) or int2 (key-major) entries
+  uint32_t* hist;     // [kCostBuckets]
+  int* counter;       // persistent-scheduler work counter
+  int n_sorted;       // number of sortable rows/units
+  int expand;         // work items per sorted row (heads sharing one list)
+};
+
+// ------------------------------------------------------------ planning (lca_plan.cu)
+void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int* kb_bounds, uint32_t* keep,
+                             int* qb_of, int* kb_of, const int* row_ptr, const int* col_idx, long long blk_nnz,
+                             size_t keep_bytes, int* status, cudaStream_t st);
+void launch_plan_fwd(const PlanView& pv, const WorkList& wl, cudaStream_t st);
+void launch_plan_dq(const PlanView& pv, const WorkList& wl, cudaStream_t st);
+void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, cudaStream_t st);
+void launch_sort(const WorkList& wl, cudaStream_t st);
+void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st);
+void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st);
+void launch_nnz(const PlanView& pv, int max_q_len, unsigned long long* acc, unsigned long long* nnz, cudaStream_t st);
+void launch_d_prepass(const void* o, const void* dout, const float* lse, float* D, float* lse2, int Tq, int Hq,
+                      cudaStream_t st);
+void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream_t st);
+void launch_probe_timeout(int* status, unsigned long long limit_ns, cudaStream_t st);
+
+// ------------------------------------------------------------ attention kernels
+struct AttnArgs {
+  PlanView pv;
+  const int* cnt;
+  const int* order;
+  const void* entries;
+  const int* list_cnt;  // dK/dV: entries per (map head, key tile) list
+  int* counter;
+  int n_work;
+  int expand;
+  int* status;
+  unsigned long long wait_limit_ns;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  // tensors
+  void* o;
+  float* lse;
+  const float* D;
+  const float* lse2;
+  void* dq;
+  void* dk;
+  void* dv;
+};
+
+void launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnArgs& a,
+                int num_sms, cudaStream_t st);
+void launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                   const AttnArgs& a, int num_sms, cudaStream_t st);
+void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
+                    const AttnArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace lca

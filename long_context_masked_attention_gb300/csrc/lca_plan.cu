@@ -1,0 +1,416 @@
+// lca_plan.cu — the mask compiler and the cost-sorted work lists, plus the
+// small HBM-bound kernels around the attention kernels.
+//
+//  * Block maps: the block-sparse CSR (LongCA-bench review, 动态掩码: uniform
+//    and variable block masks) becomes a dense keep bitmap so every kernel can
+//    test a (query block, key block) pair with one load.
+//  * Mask compiler: every (128-row query tile, 128-key tile) pair of every
+//    segment is classified EMPTY / FULL / PARTIAL and the non-empty ones are
+//    written as per-row work lists: query-major for the forward and dQ passes,
+//    key-major for the dK/dV pass.
+//  * Cost sort: the list rows are ordered by descending cost (longest first)
+//    so the persistent kernels, which claim rows through an atomic counter,
+//    balance ragged documents and shards across the SMs (FlashAttention-2's
+//    work partitioning; the disaggregation page's compute balancing).
+//  * D prepass: D_i = sum_k dO_ik O_ik, the row statistic of the backward
+//    (FlashAttention-2 核心优化, 反向传播), together with LSE in base 2.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "lca_internal.h"
+#include "sm103.cuh"
+
+namespace lca {
+
+// ---------------------------------------------------------------- block maps
+__global__ void build_keep_kernel(MaskCtx m, const int* __restrict__ row_ptr, const int* __restrict__ col_idx,
+                                  long long blk_nnz, uint32_t* keep, int* status) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rows = m.hm_count * m.n_qb;
+  if (warp >= rows) return;
+  const long long b = row_ptr[warp], e = row_ptr[warp + 1];
+  if (b < 0 || e < b || e > blk_nnz) {
+    if (lane == 0) raise_status(status, kStatusDeviceArg, 100);
+    return;
+  }
+  uint32_t* row = keep + static_cast<size_t>(warp) * m.words;
+  for (long long t = b + lane; t < e; t += 32) {
+    const int kb = col_idx[t];
+    if (kb < 0 || kb >= m.n_kb) {
+      raise_status(status, kStatusDeviceArg, 101);
+      continue;
+    }
+    atomicOr(row + (kb >> 5), 1u << (kb & 31));
+  }
+}
+
+__global__ void block_index_kernel(const int* __restrict__ bounds, int n_blocks, int T, int* map) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= n_blocks) return;
+  const int lo = bounds[b], hi = min(bounds[b + 1], T);
+  for (int t = lo; t < hi; ++t) map[t] = b;
+}
+
+void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int* kb_bounds, uint32_t* keep,
+                             int* qb_of, int* kb_of, const int* row_ptr, const int* col_idx, long long blk_nnz,
+                             size_t keep_bytes, int* status, cudaStream_t st) {
+  cudaMemsetAsync(keep, 0, keep_bytes, st);
+  const int rows = pv.mask.hm_count * pv.mask.n_qb;
+  note_launches(pv.mask.kind == kBlockSparseVariable ? 3 : 1);
+  build_keep_kernel<<<(rows + 7) / 8, 256, 0, st>>>(pv.mask, row_ptr, col_idx, blk_nnz, keep, status);
+  if (pv.mask.kind == kBlockSparseVariable) {
+    block_index_kernel<<<(pv.mask.n_qb + 127) / 128, 128, 0, st>>>(qb_bounds, pv.mask.n_qb, pv.Tq, qb_of);
+    block_index_kernel<<<(pv.mask.n_kb + 127) / 128, 128, 0, st>>>(kb_bounds, pv.mask.n_kb, pv.Tk, kb_of);
+  }
+}
+
+// ---------------------------------------------------------------- query-major lists
+// One warp per list row (map head, segment, query block of SUB*128 rows).
+// Entry = key tile index | class of sub-tile 0 << 24 | class of sub-tile 1 << 26.
+template <int SUB>
+__global__ void plan_q_rows_kernel(PlanView pv, int* __restrict__ cnt, uint32_t* __restrict__ entries,
+                                   uint32_t* __restrict__ hist) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int R = (SUB == 2) ? pv.R256 : pv.R128;
+  if (row >= pv.hm_count * R) return;
+  const int hm = row / R, rr = row % R;
+  const int* qstart = (SUB == 2) ? pv.q256_start : pv.q128_start;
+  const int s = find_bucket(qstart, pv.n_seg, rr);
+  const SegInfo sg = pv.segs[s];
+  const int qb = rr - qstart[s];
+  const long long per_hm = (SUB == 2) ? pv.fwd_per_hm : pv.dq_per_hm;
+  const long long off = (SUB == 2) ? pv.fwd_off[s] : pv.dq_off[s];
+  uint32_t* out = entries + hm * per_hm + off + static_cast<long long>(qb) * sg.nk;
+  int n = 0;
+  for (int kt = 0; kt < sg.nk; ++kt) {
+    const uint32_t c0 = classify_tile_warp(pv.mask, sg, hm, qb * SUB * kTile, kt * kTile);
+    const uint32_t c1 = (SUB == 2) ? classify_tile_warp(pv.mask, sg, hm, qb * SUB * kTile + kTile, kt * kTile) : 0u;
+    if (c0 | c1) {
+      if (lane == 0) out[n] = static_cast<uint32_t>(kt) | (c0 << 24) | (c1 << 26);
+      ++n;
+    }
+  }
+  if (lane == 0) {
+    cnt[row] = n;
+    atomicAdd(hist + min(n, kCostBuckets - 1), 1u);
+  }
+}
+
+void launch_plan_fwd(const PlanView& pv, const WorkList& wl, cudaStream_t st) {
+  const int rows = pv.hm_count * pv.R256;
+  if (rows == 0) return;
+  note_launches(1);
+  plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, wl.cnt, static_cast<uint32_t*>(wl.entries), wl.hist);
+}
+
+void launch_plan_dq(const PlanView& pv, const WorkList& wl, cudaStream_t st) {
+  const int rows = pv.hm_count * pv.R128;
+  if (rows == 0) return;
+  note_launches(1);
+  plan_q_rows_kernel<1><<<(rows + 7) / 8, 256, 0, st>>>(pv, wl.cnt, static_cast<uint32_t*>(wl.entries), wl.hist);
+}
+
+// ---------------------------------------------------------------- key-major lists
+// One warp per unit (map KV head gm, key group, key tile).  For a shared map
+// (H' = 1) the unit has one list; for per-head maps it has one list per query
+// head of the KV head.  Entry = {segment, query tile | class << 24}.
+__global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* __restrict__ list_cnt,
+                                     int2* __restrict__ entries, uint32_t* __restrict__ hist, int n_units) {
+  const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (unit >= n_units) return;
+  const int gm = unit / pv.RK, rk = unit % pv.RK;
+  const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
+  const KeyGroup grp = pv.kgs[kg];
+  const int kt = rk - pv.kt_start[kg];
+  const int nlists = (pv.hm_count == 1) ? 1 : pv.G;
+  int cost = 0;
+  for (int l = 0; l < nlists; ++l) {
+    const int hm = (pv.hm_count == 1) ? 0 : gm * pv.G + l;
+    int2* out = entries + hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(kt) * grp.pairs;
+    int n = 0;
+    for (int si = grp.seg_begin; si < grp.seg_end; ++si) {
+      const int s = pv.kg_segs[si];
+      const SegInfo sg = pv.segs[s];
+      if (kt * kTile >= sg.k_len) continue;
+      const int nq = (sg.q_len + kTile - 1) / kTile;
+      for (int qt = 0; qt < nq; ++qt) {
+        const uint32_t c = classify_tile_warp(pv.mask, sg, hm, qt * kTile, kt * kTile);
+        if (c) {
+          if (lane == 0) out[n] = make_int2(s, qt | static_cast<int>(c << 24));
+          ++n;
+        }
+      }
+    }
+    if (lane == 0) list_cnt[hm * pv.RK + rk] = n;
+    cost += n;
+  }
+  if (lane == 0) {
+    ucnt[unit] = cost;
+    atomicAdd(hist + min(cost, kCostBuckets - 1), 1u);
+  }
+}
+
+void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, cudaStream_t st) {
+  const int n_units = wl.n_sorted;
+  if (n_units == 0) return;
+  note_launches(1);
+  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, wl.cnt, list_cnt, static_cast<int2*>(wl.entries),
+                                                          wl.hist, n_units);
+}
+
+// ---------------------------------------------------------------- cost sort
+// Counting sort by descending cost in one block of 1024 threads.  Rows with
+// equal cost keep no particular order (the result does not depend on it).
+__global__ void __launch_bounds__(1024) sort_kernel(const int* __restrict__ cnt, int n, const uint32_t* __restrict__ hist,
+                                                    int* __restrict__ order, int* __restrict__ counter) {
+  __shared__ uint32_t start[kCostBuckets];
+  __shared__ uint32_t warp_sums[32];
+  const int tid = threadIdx.x;
+  constexpr int kPer = kCostBuckets / 1024;  // buckets per thread
+  // position p = 0 is the most expensive bucket
+  uint32_t local[kPer];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    local[t] = hist[kCostBuckets - 1 - (tid * kPer + t)];
+    sum += local[t];
+  }
+  // exclusive scan of `sum` over the block
+  uint32_t incl = sum;
+  const int lane = tid & 31, wid = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) warp_sums[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t w = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, w, o);
+      if (lane >= o) w += v;
+    }
+    warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  uint32_t run = incl - sum + (wid > 0 ? warp_sums[wid - 1] : 0u);
+#pragma unroll
+  for (int t = 0; t < kPer; ++t) {
+    start[kCostBuckets - 1 - (tid * kPer + t)] = run;
+    run += local[t];
+  }
+  __syncthreads();
+  for (int r = tid; r < n; r += blockDim.x) {
+    const int b = min(cnt[r], kCostBuckets - 1);
+    const uint32_t pos = atomicAdd(&start[b], 1u);
+    order[pos] = r;
+  }
+  if (tid == 0) *counter = 0;
+}
+
+void launch_sort(const WorkList& wl, cudaStream_t st) {
+  note_launches(1);
+  sort_kernel<<<1, 1024, 0, st>>>(wl.cnt, wl.n_sorted, wl.hist, wl.order, wl.counter);
+}
+
+// ---------------------------------------------------------------- test hooks
+__global__ void materialize_seg_kernel(PlanView pv, int seg, int hm, uint8_t* __restrict__ out) {
+  const SegInfo sg = pv.segs[seg];
+  const int nch = (sg.k_len + 31) / 32;
+  const long long total = static_cast<long long>(sg.q_len) * nch;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(idx / nch);
+    const int c = static_cast<int>(idx % nch);
+    const uint32_t bits = mask_bits(pv.mask, sg, hm, i, c * 32);
+    uint8_t* row = out + static_cast<long long>(i) * sg.k_len;
+    for (int t = 0; t < 32; ++t) {
+      const int j = c * 32 + t;
+      if (j < sg.k_len) row[j] = static_cast<uint8_t>((bits >> t) & 1u);
+    }
+  }
+}
+
+__global__ void tile_classes_kernel(PlanView pv, int seg, int hm, uint8_t* __restrict__ out) {
+  const SegInfo sg = pv.segs[seg];
+  const int nq = (sg.q_len + kTile - 1) / kTile;
+  const int tile = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (tile >= nq * sg.nk) return;
+  const int qt = tile / sg.nk, kt = tile % sg.nk;
+  const uint32_t c = classify_tile_warp(pv.mask, sg, hm, qt * kTile, kt * kTile);
+  if ((threadIdx.x & 31) == 0) out[tile] = static_cast<uint8_t>(c);
+}
+
+// nnz: interval families — one thread per query row, grid.y = segment.
+__global__ void nnz_rows_kernel(PlanView pv, unsigned long long* acc) {
+  const int s = blockIdx.y;
+  const SegInfo sg = pv.segs[s];
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  unsigned long long n = 0;
+  if (i < sg.q_len) n = static_cast<unsigned long long>(span_count(row_span(pv.mask, sg, i)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+  if ((threadIdx.x & 31) == 0 && n) atomicAdd(acc, n);
+}
+
+// nnz: block-sparse — one thread per CSR row (map head, query block).
+__global__ void nnz_blocks_kernel(PlanView pv, unsigned long long* acc) {
+  const MaskCtx& m = pv.mask;
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= m.hm_count * m.n_qb) return;
+  const int hm = r / m.n_qb, qb = r % m.n_qb;
+  const long long qs = (m.kind == kBlockSparseUniform) ? static_cast<long long>(qb) * m.q_block : -1;
+  unsigned long long n = 0;
+  for (int s = 0; s < pv.n_seg; ++s) {
+    const SegInfo sg = pv.segs[s];
+    // rows of this query block inside the segment
+    const long long q0 = (m.kind == kBlockSparseUniform) ? qs : m.qb_start[qb];
+    const long long q1 = (m.kind == kBlockSparseUniform) ? qs + m.q_block : m.qb_start[qb + 1];
+    const long long r_lo = max(q0, static_cast<long long>(sg.q_off));
+    const long long r_hi = min(q1, static_cast<long long>(sg.q_off + sg.q_len));
+    if (r_hi <= r_lo) continue;
+    const long long rows = r_hi - r_lo;
+    for (int kb = 0; kb < m.n_kb; ++kb) {
+      if (!block_kept(m, hm, qb, kb)) continue;
+      const int k0 = k_block_start(m, kb);
+      const int k1 = (m.kind == kBlockSparseUniform) ? k0 + m.kv_block : m.kb_start[kb + 1];
+      const int c_lo = max(k0, sg.k_off), c_hi = min(k1, sg.k_off + sg.k_len);
+      if (c_hi > c_lo) n += static_cast<unsigned long long>(rows) * (c_hi - c_lo);
+    }
+  }
+  if (n) atomicAdd(acc + hm, n);
+}
+
+__global__ void nnz_broadcast_kernel(const unsigned long long* acc, int hm_count, int Hq, unsigned long long* nnz) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < Hq) nnz[h] = acc[hm_count == 1 ? 0 : h];
+}
+
+void launch_nnz(const PlanView& pv, int max_q_len, unsigned long long* acc, unsigned long long* nnz, cudaStream_t st) {
+  if (is_block_sparse(pv.mask.kind)) {
+    const int rows = pv.mask.hm_count * pv.mask.n_qb;
+    if (rows > 0) nnz_blocks_kernel<<<(rows + 127) / 128, 128, 0, st>>>(pv, acc);
+  } else if (pv.n_seg > 0 && max_q_len > 0) {
+    dim3 grid((max_q_len + 255) / 256, pv.n_seg);
+    nnz_rows_kernel<<<grid, 256, 0, st>>>(pv, acc);
+  }
+  nnz_broadcast_kernel<<<(pv.Hq + 127) / 128, 128, 0, st>>>(acc, pv.hm_count, pv.Hq, nnz);
+  note_launches(2);
+}
+
+void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st) {
+  const long long chunks = (cells + 31) / 32 + 1;
+  const int blocks = static_cast<int>(min(65535LL, (chunks + 255) / 256));
+  note_launches(1);
+  materialize_seg_kernel<<<max(blocks, 1), 256, 0, st>>>(pv, seg, hm, out);
+}
+
+void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st) {
+  if (tiles == 0) return;
+  note_launches(1);
+  tile_classes_kernel<<<(tiles + 7) / 8, 256, 0, st>>>(pv, seg, hm, out);
+}
+
+// ---------------------------------------------------------------- D prepass
+// One block per (head, 64 rows).  Each half-warp reads one 256-byte row of O
+// and of dO (16 lanes x 16 bytes), so every load is a full sector.
+__global__ void __launch_bounds__(256) d_prepass_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                                        const float* __restrict__ lse, float* __restrict__ D,
+                                                        float* __restrict__ lse2, int Tq, int Hq) {
+  const int h = blockIdx.y;
+  const int t0 = blockIdx.x * 64;
+  const int hw = threadIdx.x >> 4;  // half-warp 0..15
+  const int l16 = threadIdx.x & 15;
+  float acc[4];
+  uint4 a[4], b[4];
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int t = t0 + it * 16 + hw;
+    if (t < Tq) {
+      const size_t base = (static_cast<size_t>(t) * Hq + h) * 16 + l16;  // 16 uint4 per 128-element row
+      a[it] = __ldg(o + base);
+      b[it] = __ldg(dout + base);
+    } else {
+      a[it] = make_uint4(0, 0, 0, 0);
+      b[it] = make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a[it]);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b[it]);
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 x = __bfloat1622float2(pa[u]);
+      const float2 y = __bfloat1622float2(pb[u]);
+      s = fmaf(x.x, y.x, s);
+      s = fmaf(x.y, y.y, s);
+    }
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off, 16);
+    acc[it] = s;
+  }
+  if (l16 == 0) {
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int t = t0 + it * 16 + hw;
+      if (t < Tq) {
+        const size_t idx = static_cast<size_t>(h) * Tq + t;
+        D[idx] = acc[it];
+        const float l = lse[idx];
+        // log2-domain LSE; a row with no key (-inf) gets +inf so that P = 0
+        lse2[idx] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+      }
+    }
+  }
+}
+
+void launch_d_prepass(const void* o, const void* dout, const float* lse, float* D, float* lse2, int Tq, int Hq,
+                      cudaStream_t st) {
+  if (Tq == 0) return;
+  dim3 grid((Tq + 63) / 64, Hq);
+  note_launches(1);
+  d_prepass_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, D, lse2,
+                                         Tq, Hq);
+}
+
+__global__ void fill_lse_kernel(float* lse, int Tq, int Hq, int row0, int nrows) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(nrows) * Hq) return;
+  const int h = static_cast<int>(idx / nrows), r = static_cast<int>(idx % nrows);
+  lse[static_cast<size_t>(h) * Tq + row0 + r] = -INFINITY;
+}
+
+void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream_t st) {
+  const long long n = static_cast<long long>(nrows) * Hq;
+  if (n == 0) return;
+  note_launches(1);
+  fill_lse_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, st>>>(lse, Tq, Hq, row0, nrows);
+}
+
+// ---------------------------------------------------------------- timeout probe
+__global__ void probe_timeout_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Nothing ever arrives on `bar`: the bounded wait must give up and record
+  // LCA_ERR_TIMEOUT.
+  mbar_wait(&bar, 0, status, limit_ns, kStatusTimeout, 900);
+  __syncthreads();
+}
+
+void launch_probe_timeout(int* status, unsigned long long limit_ns, cudaStream_t st) {
+  note_launches(1);
+  probe_timeout_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+}
+
+}  // namespace lca
