@@ -177,6 +177,10 @@ LCA_API lca_status lca_probe_wait_timeout(void* workspace, size_t workspace_byte
  * entries, may be null).  Pass null to stop.  Process-wide, not thread-safe. */
 LCA_API lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases);
 
+/* Text of the last CUDA failure seen by this library in the calling thread
+ * (the failing call and the runtime's message), or "" if none. */
+LCA_API const char* lca_last_error_detail(void);
+
 /* Number of kernels this library has launched since it was loaded. */
 LCA_API uint64_t lca_launch_count(void);
 

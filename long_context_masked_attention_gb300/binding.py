@@ -25,7 +25,7 @@ STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "L
           4: "LCA_ERR_CUDA", 5: "LCA_ERR_TIMEOUT", 6: "LCA_ERR_DEVICE_ARG"}
 EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
             "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
-            "lca_status_string", "lca_version")
+            "lca_last_error_detail", "lca_status_string", "lca_version")
 PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
 
 
@@ -89,11 +89,13 @@ def load(path: str = LIB_PATH):
     lib.lca_set_kernel_events.argtypes = [C.POINTER(C.c_void_p), C.c_int32, C.POINTER(C.c_int32)]
     lib.lca_launch_count.restype = C.c_uint64
     lib.lca_launch_count.argtypes = []
+    lib.lca_last_error_detail.restype = C.c_char_p
+    lib.lca_last_error_detail.argtypes = []
     lib.lca_status_string.argtypes = [st]
     lib.lca_status_string.restype = C.c_char_p
     lib.lca_version.restype = C.c_int32
     for name in EXPORTED:
-        if name not in ("lca_status_string", "lca_version", "lca_launch_count"):
+        if name not in ("lca_status_string", "lca_version", "lca_launch_count", "lca_last_error_detail"):
             getattr(lib, name).restype = st
     _lib = lib
     return lib
@@ -194,6 +196,8 @@ def marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale=0.0, device=None) -> Call:
 
 def _check(code, what):
     if code != 0:
+        if code == 4:
+            what += " (" + load().lca_last_error_detail().decode() + ")"
         raise LcaError(code, what)
 
 
@@ -308,6 +312,9 @@ class KernelEvents:
         import torch
 
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_pairs)]
+        for e in self.events:  # torch creates the CUDA event lazily, on first record
+            e.record()
+        torch.cuda.synchronize()
         self._arr = (C.c_void_p * (2 * n_pairs))(*[e.cuda_event for e in self.events])
         self._ph = (C.c_int32 * n_pairs)(*([-1] * n_pairs))
         self.n_pairs = n_pairs

@@ -9,6 +9,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -23,6 +24,13 @@ static std::atomic<unsigned long long> g_launches{0};
 void note_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n), std::memory_order_relaxed); }
 
 namespace {
+
+thread_local char g_err_detail[256] = "";
+
+lca_status cuda_fail(const char* what, cudaError_t e) {
+  snprintf(g_err_detail, sizeof(g_err_detail), "%s: %s", what, cudaGetErrorString(e));
+  return LCA_ERR_CUDA;
+}
 
 // Profiling ring (lca_set_kernel_events).
 struct EventRing {
@@ -39,11 +47,14 @@ int phase_begin(int phase, cudaStream_t st) {
   const int p = g_ring.cursor;
   g_ring.cursor = (g_ring.cursor + 1) % g_ring.n_pairs;
   if (g_ring.phases) g_ring.phases[p] = phase;
-  cudaEventRecord(static_cast<cudaEvent_t>(g_ring.events[2 * p]), st);
+  // a failed record must not leak into the call's own error checks
+  if (cudaEventRecord(static_cast<cudaEvent_t>(g_ring.events[2 * p]), st) != cudaSuccess) (void)cudaGetLastError();
   return p;
 }
 void phase_end(int p, cudaStream_t st) {
-  if (p >= 0) cudaEventRecord(static_cast<cudaEvent_t>(g_ring.events[2 * p + 1]), st);
+  if (p < 0) return;
+  if (cudaEventRecord(static_cast<cudaEvent_t>(g_ring.events[2 * p + 1]), st) != cudaSuccess)
+    (void)cudaGetLastError();
 }
 
 constexpr size_t kAlign = 256;
@@ -405,20 +416,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [rows][heads * 128] bf16, 64-column x box_rows boxes, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* ptr, int rows, int heads, int box_rows) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn) {
+    snprintf(g_err_detail, sizeof(g_err_detail), "cuTensorMapEncodeTiled entry point unavailable");
+    return false;
+  }
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads) * kHeadDim, static_cast<cuuint64_t>(std::max(rows, 1))};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads) * kHeadDim * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    snprintf(g_err_detail, sizeof(g_err_detail), "cuTensorMapEncodeTiled(rows=%d, heads=%d, box_rows=%d): CUresult %d",
+             rows, heads, box_rows, static_cast<int>(r));
+  return r == CUDA_SUCCESS;
 }
 
 int num_sms() {
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    cuda_fail("cudaDeviceGetAttribute(multiProcessorCount)", e);
+    return 0;
+  }
   return n;
 }
 
@@ -434,9 +456,11 @@ unsigned long long wait_limit_ns() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-#define LCA_CUDA(x)                                    \
-  do {                                                 \
-    if ((x) != cudaSuccess) return LCA_ERR_CUDA;       \
+
+#define LCA_CUDA(x)                                  \
+  do {                                               \
+    const cudaError_t e_ = (x);                      \
+    if (e_ != cudaSuccess) return cuda_fail(#x, e_); \
   } while (0)
 
 // Common preamble of every entry point that launches: validate, lay out,
@@ -511,12 +535,16 @@ int32_t lca_version(void) { return 100; }
 
 lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases) {
   if (events && (n_events < 2 || (n_events & 1))) return LCA_ERR_INVALID_ARG;
+  for (int32_t i = 0; events && i < n_events; ++i)
+    if (!events[i]) return LCA_ERR_INVALID_ARG;  // every handle must be a created event
   g_ring.events = events;
   g_ring.phases = phases;
   g_ring.n_pairs = events ? n_events / 2 : 0;
   g_ring.cursor = 0;
   return LCA_OK;
 }
+
+const char* lca_last_error_detail(void) { return g_err_detail; }
 
 uint64_t lca_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
