@@ -45,10 +45,11 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_problems():
+def workload_problems(only=None):
     from gen import STATIC_KINDS, config2
 
-    return [config2(k) for k in STATIC_KINDS]
+    kinds = [k for k in STATIC_KINDS if only is None or k in only.split(",")]
+    return [config2(k) for k in kinds]
 
 
 # ------------------------------------------------------------------ clocks
@@ -227,7 +228,7 @@ def run_ours(args):
             dist.barrier()
 
     lca.load()
-    probs = workload_problems()
+    probs = workload_problems(args.only)
     p0 = probs[0]
     q, k, v, do = make_tensors(p0, device=dev)
     calls = [lca.marshal(p.Tq, p.Tk, p.Hq, p.Hkv, p.d, p.segments, p.mask, p.scale) for p in probs]
@@ -368,6 +369,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, help="comma-separated mask kinds (profiling runs; not a bench line)")
     ap.add_argument("--_oracle_sample", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args._oracle_sample is not None:
