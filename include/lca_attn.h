@@ -156,6 +156,29 @@ LCA_API lca_status lca_mask_tile_classes(const lca_shape* shape, const lca_mask_
 LCA_API lca_status lca_mask_nnz(const lca_shape* shape, const lca_mask_desc* mask, uint64_t* nnz, void* workspace,
                         size_t workspace_bytes, void* stream);
 
+/* Forward pass with a library-owned workspace, for callers that cannot
+ * allocate device memory: processes whose device-memory pool was carved out
+ * up front and may not grow, or code running where an allocation is not
+ * allowed (inside an allocator's own callback, for example).  The pages have
+ * no counterpart: this is a deployment convenience of this library.
+ * Arguments and results are those of lca_attn_fwd; the caller still passes
+ * (and owns) q, k, v, o and lse.
+ * Scratch: one static device array of LCA_STATIC_WORKSPACE_BYTES (16 MiB),
+ * which every GPU that loads this library holds until the process exits.  A
+ * shape whose forward workspace (lca_workspace_size with for_bwd = 0) is
+ * larger is rejected with LCA_ERR_WORKSPACE before anything is launched, and
+ * lca_last_error_detail says how much it needed.
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Every call on a device shares the one array and clears what must start at
+ * zero; calls that overlap on the GPU (two streams, or two host threads)
+ * race on it, so the caller must serialise them.
+ * No device memory is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine is called. */
+#define LCA_STATIC_WORKSPACE_BYTES (16u << 20)
+LCA_API lca_status lca_attn_fwd_static_workspace(const void* q, const void* k, const void* v, void* o, float* lse,
+                                                 const lca_shape* shape, const lca_mask_desc* mask, void* stream);
+
 /* Synchronises `stream`, then copies the device status word of the last
  * call that used this workspace: out[0] = lca_status code (0 = none),
  * out[1] = where it was raised.  Each fwd/bwd call clears it first. */

@@ -25,7 +25,7 @@ STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "L
           4: "LCA_ERR_CUDA", 5: "LCA_ERR_TIMEOUT", 6: "LCA_ERR_DEVICE_ARG"}
 EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
             "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
-            "lca_last_error_detail", "lca_status_string", "lca_version")
+            "lca_last_error_detail", "lca_attn_fwd_static_workspace", "lca_status_string", "lca_version")
 PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
 
 
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH):
     lib.lca_set_kernel_events.argtypes = [C.POINTER(C.c_void_p), C.c_int32, C.POINTER(C.c_int32)]
     lib.lca_launch_count.restype = C.c_uint64
     lib.lca_launch_count.argtypes = []
+    lib.lca_attn_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp]
     lib.lca_last_error_detail.restype = C.c_char_p
     lib.lca_last_error_detail.argtypes = []
     lib.lca_status_string.argtypes = [st]

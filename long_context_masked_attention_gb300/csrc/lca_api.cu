@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <vector>
 
 #include "../../include/lca_attn.h"
@@ -774,3 +775,41 @@ lca_status lca_probe_wait_timeout(void* workspace, size_t workspace_bytes, int32
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ static workspace
+// The workspace of lca_attn_fwd_static_workspace: a file-scope device array.
+// Host code must not use the symbol itself (on the host it is only a
+// stand-in); it uses the device address looked up once per device.
+static __device__ __align__(256) unsigned char g_static_workspace[LCA_STATIC_WORKSPACE_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+void* g_static_ws_ptr[kMaxDevices] = {};
+std::mutex g_static_ws_mu;
+}  // namespace
+
+extern "C" lca_status lca_attn_fwd_static_workspace(const void* q, const void* k, const void* v, void* o, float* lse,
+                                                    const lca_shape* shape, const lca_mask_desc* mask, void* stream) {
+  size_t need = 0;
+  const lca_status r = lca_workspace_size(shape, mask, 0, &need);
+  if (r != LCA_OK) return r;
+  if (need > LCA_STATIC_WORKSPACE_BYTES) {
+    snprintf(g_err_detail, sizeof(g_err_detail), "forward needs %zu workspace bytes; the static workspace holds %u",
+             need, LCA_STATIC_WORKSPACE_BYTES);
+    return LCA_ERR_WORKSPACE;
+  }
+  int dev = -1;
+  LCA_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return LCA_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_ws_mu);
+    if (!g_static_ws_ptr[dev]) {
+      void* p = nullptr;
+      LCA_CUDA(cudaGetSymbolAddress(&p, g_static_workspace));  // with device `dev` current
+      g_static_ws_ptr[dev] = p;
+    }
+    ws = g_static_ws_ptr[dev];
+  }
+  return lca_attn_fwd(q, k, v, o, lse, shape, mask, ws, LCA_STATIC_WORKSPACE_BYTES, stream);
+}
