@@ -92,7 +92,8 @@ struct Layout {
          b_parts = 0, b_qbb = 0, b_kbb = 0;
   size_t keep = 0, keep_bytes = 0, qb_of = 0, kb_of = 0;
   size_t f_cnt = 0, f_order = 0, f_ent = 0;
-  size_t D = 0, lse2 = 0, q_cnt = 0, q_order = 0, q_ent = 0, k_ucnt = 0, k_order = 0, k_lcnt = 0, k_ent = 0;
+  size_t D = 0, lse2 = 0, q_cnt = 0, q_order = 0, q_ent = 0, k_ucnt = 0, k_order = 0, k_lcnt = 0, k_lsteps = 0,
+         k_ent = 0;
   size_t total = 0;
 };
 
@@ -337,6 +338,7 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     L.k_ucnt = take(sizeof(int) * std::max<size_t>(1, hkv_m * P.RK));
     L.k_order = take(sizeof(int) * std::max<size_t>(1, hkv_m * P.RK));
     L.k_lcnt = take(sizeof(int) * std::max<size_t>(1, H * P.RK));
+    L.k_lsteps = take(sizeof(int) * std::max<size_t>(1, H * P.RK));
     L.k_ent = take(sizeof(int2) * std::max<size_t>(1, H * P.dkv_per_hm));
   }
   L.total = o;
@@ -656,8 +658,9 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     wl.n_sorted = static_cast<int>(k_units);
     wl.expand = P.Hkv / hkv_m;
     int* list_cnt = reinterpret_cast<int*>(c.ws + c.L.k_lcnt);
+    int* list_steps = reinterpret_cast<int*>(c.ws + c.L.k_lsteps);
     ph = phase_begin(3, c.st);
-    launch_plan_dkv(c.V, wl, list_cnt, c.st);
+    launch_plan_dkv(c.V, wl, list_cnt, list_steps, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
     AttnArgs a = base_args(c);
@@ -665,6 +668,7 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     a.order = wl.order;
     a.entries = wl.entries;
     a.list_cnt = list_cnt;
+    a.list_steps = list_steps;
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(k_units * wl.expand);

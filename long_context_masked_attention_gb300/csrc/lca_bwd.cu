@@ -243,8 +243,10 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
     const float lse2 = valid ? a.lse2[stat] : INFINITY;
     const float Dv = valid ? a.D[stat] : 0.f;
+    uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
     for (int t = 0; t < inf.cnt; ++t) {
-      const uint32_t e = entries[inf.ebase + t];
+      const uint32_t e = e_next;  // the next entry's load overlaps this tile's work
+      if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
       const uint32_t cls = (e >> 24) & 3u;
       const int kt = static_cast<int>(e & 0xFFFFFFu);
       if (!waitw(&bar[B_SFULL], sdp & 1, a, 131)) return;
@@ -269,8 +271,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         for (int c = 0; c < 2; ++c) {
           const uint32_t bits = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (!((bits >> k) & 1u)) s[32 * c + k] = -INFINITY;
+          for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
         }
       }
       uint32_t pk[32];
@@ -362,21 +363,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ====================================================================== dK / dV
 namespace dkv {
 
+constexpr int kRing = 3;                        // Q/dO (and staged statistics) ring depth
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTile128;
-constexpr int kOffQ = kOffV + kTile128;     // 2-slot ring of 64-row Q tiles
-constexpr int kOffDO = kOffQ + 2 * kTile64; // 2-slot ring of 64-row dO tiles
-constexpr int kOffP = kOffDO + 2 * kTile64; // 2 buffers of P^T  [128 keys x 64 queries]
-constexpr int kOffDS = kOffP + 2 * kTile64; // 2 buffers of dS^T
-constexpr int kOffStat = kOffDS + 2 * kTile64;  // 2 buffers of: lse2[64], D[64], mask words[64][4]
-constexpr int kStatBytes = 64 * 4 * 2 + 64 * 4 * 4;
-constexpr int kOffCtl = kOffStat + 2 * kStatBytes;
+constexpr int kOffQ = kOffV + kTile128;          // ring of 64-row Q tiles
+constexpr int kOffDO = kOffQ + kRing * kTile64;  // ring of 64-row dO tiles
+constexpr int kOffP = kOffDO + kRing * kTile64;  // P^T  [128 keys x 64 queries]
+constexpr int kOffDS = kOffP + kTile64;          // dS^T
+constexpr int kOffStat = kOffDS + kTile64;       // kRing buffers of: lse2[64], D[64], mask words[64][4], meta
+constexpr int kStatBytes = 64 * 4 * 2 + 64 * 4 * 4 + 16;
+constexpr int kOffCtl = kOffStat + kRing * kStatBytes;
 constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
 
 enum : int {
-  B_KVFULL = 0, B_KVEMPTY, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_SFULL1, B_SEMPTY, B_SEMPTY1,
-  B_PFULL, B_PFULL1, B_PEMPTY, B_PEMPTY1, B_ACCFULL, B_ITFULL, B_ITFULL1, B_ITEMPTY, B_ITEMPTY1, B_DRAIN, B_STAT,
-  B_COUNT
+  B_KVFULL = 0, B_KVEMPTY,
+  B_QFULL, B_QEMPTY = B_QFULL + kRing, B_MFULL = B_QEMPTY + kRing, B_MEMPTY = B_MFULL + kRing,
+  B_SFULL = B_MEMPTY + kRing, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY, B_ACCFULL,
+  B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_DRAIN = B_ITEMPTY + 2, B_COUNT
 };
 
 struct Item {
@@ -384,96 +387,51 @@ struct Item {
   int rk, pad;
 };
 
-// Steps of an item: for each query head of the KV head, each entry of its
-// list, each 64-row half of the 128-row query tile that lies inside the
-// segment.  Every role walks them in the same order.
-struct StepIter {
-  const AttnArgs* a;
-  int g, rk;
-  int l, e, half, n_in_list;
-  long long ebase;
-  __device__ void start(const AttnArgs& args, int g_, int kg, int kt, int rk_) {
-    a = &args;
-    g = g_;
-    rk = rk_;
-    l = -1;
-    e = 0;
-    half = 0;
-    n_in_list = 0;
-    (void)kg;
-    (void)kt;
-    next_list();
-  }
-  __device__ void next_list() {
-    const PlanView& pv = a->pv;
-    while (true) {
-      ++l;
-      if (l >= pv.G) return;
-      const int hm = (pv.hm_count == 1) ? 0 : g * pv.G + l;
-      const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
-      const KeyGroup grp = pv.kgs[kg];
-      const int kt = rk - pv.kt_start[kg];
-      n_in_list = a->list_cnt[hm * pv.RK + rk];
-      ebase = hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(kt) * grp.pairs;
-      e = 0;
-      half = 0;
-      if (n_in_list > 0) return;
-    }
-  }
-  // Returns false when done; otherwise the step's segment, head, first query row and class.
-  __device__ bool next(int& seg, int& head, int& r0, uint32_t& cls) {
-    const PlanView& pv = a->pv;
-    const int2* entries = static_cast<const int2*>(a->entries);
-    while (l < pv.G) {
-      if (e >= n_in_list) {
-        next_list();
-        continue;
-      }
-      const int2 en = entries[ebase + e];
-      const int s = en.x;
-      const int qt = en.y & 0xFFFFFF;
-      const int h = half;
-      if (++half == 2) {
-        half = 0;
-        ++e;
-      }
-      const int q_len = pv.segs[s].q_len;
-      const int rr = qt * kTile + 64 * h;
-      if (rr >= q_len) continue;
-      seg = s;
-      head = g * pv.G + l;
-      r0 = rr;
-      cls = static_cast<uint32_t>(en.y >> 24) & 3u;
-      return true;
-    }
-    return false;
-  }
+// Per-step data the producer warp stages for the compute warps (buffer b of
+// two): the 64 query rows' LSE (base 2) and D, the mask words of a partial
+// tile, and the step's class.  The compute warps read only shared memory.
+struct StepMeta {
+  int cls, pad0, pad1, pad2;
 };
-
-__device__ __forceinline__ int count_steps(const AttnArgs& a, int g, int rk) {
-  StepIter si;
-  si.start(a, g, 0, 0, rk);
-  int n = 0, s, h, r0;
-  uint32_t c;
-  while (si.next(s, h, r0, c)) ++n;
-  return n;
+__device__ __forceinline__ float* stat_lse2(uint8_t* sm, int b) {
+  return reinterpret_cast<float*>(sm + kOffStat + b * kStatBytes);
+}
+__device__ __forceinline__ float* stat_D(uint8_t* sm, int b) { return stat_lse2(sm, b) + 64; }
+__device__ __forceinline__ uint32_t* stat_mask(uint8_t* sm, int b) {
+  return reinterpret_cast<uint32_t*>(stat_lse2(sm, b) + 128);
+}
+__device__ __forceinline__ StepMeta* stat_meta(uint8_t* sm, int b) {
+  return reinterpret_cast<StepMeta*>(stat_mask(sm, b) + 256);
 }
 
+// The whole producer warp runs this loop; lane 0 issues the TMA copies and
+// the barrier arrivals, all lanes fetch list entries (32 at a time, so one
+// memory latency covers 32 entries) and stage the per-step statistics with
+// cp.async, whose completion the step's barrier tracks.
+//
+// Steps of an item: for each query head of the KV head, each entry of its
+// list, each 64-row half of the 128-row query tile that lies inside the
+// segment.
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
                                          Item* items) {
   const PlanView& pv = a.pv;
+  const int2* entries = static_cast<const int2*>(a.entries);
+  const int lane = threadIdx.x & 31;
   uint32_t steps = 0;
   int kv_issued = 0;
   int it = 0;
   for (;; ++it) {
     const int slot = it & 1;
-    if (it >= 2 && !wait1(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 210)) goto abort;
+    if (it >= 2 && !waitw(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 210)) goto abort;
     {
-      const int w = atomicAdd(a.counter, 1);
+      int w = 0;
+      if (lane == 0) w = atomicAdd(a.counter, 1);
+      w = __shfl_sync(0xFFFFFFFFu, w, 0);
       Item inf;
       inf.valid = 0;
       if (w < a.n_work) {
+        // consecutive items: the KV heads of one unit, so the cost order (longest first) holds across heads
         const int unit = a.order[w / a.expand];
         const int gm = unit / pv.RK, rk = unit % pv.RK;
         const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
@@ -483,43 +441,115 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         inf.rk = rk;
         inf.g = (pv.hm_count == 1) ? (w % a.expand) : gm;
         inf.unit_hm = 0;
-        inf.nsteps = count_steps(a, inf.g, rk);
+        int n = 0;
+        if (pv.hm_count == 1) {
+          n = pv.G * a.list_steps[rk];
+        } else {
+          for (int l = 0; l < pv.G; ++l) n += a.list_steps[(inf.g * pv.G + l) * pv.RK + rk];
+        }
+        inf.nsteps = n;
       }
-      items[slot] = inf;
-      mbar_arrive(&bar[B_ITFULL + slot]);
+      if (lane == 0) {
+        items[slot] = inf;
+        mbar_arrive(&bar[B_ITFULL + slot]);
+      }
       if (!inf.valid) return;
       const KeyGroup grp = pv.kgs[inf.kg];
       const int yk = grp.k_off + inf.kt * kTile;
-      if (it >= 1 && !wait1(&bar[B_KVEMPTY], (it - 1) & 1, a, 211)) goto abort;
-      mbar_arrive_expect_tx(&bar[B_KVFULL], 2 * kTile128);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_2d(sm + kOffK + c * kChunk128, tk, &bar[B_KVFULL], inf.g * kHeadDim + c * 64, yk);
-        tma_load_2d(sm + kOffV + c * kChunk128, tv, &bar[B_KVFULL], inf.g * kHeadDim + c * 64, yk);
+      if (it >= 1 && !waitw(&bar[B_KVEMPTY], (it - 1) & 1, a, 211)) goto abort;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar[B_KVFULL], 2 * kTile128);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(sm + kOffK + c * kChunk128, tk, &bar[B_KVFULL], inf.g * kHeadDim + c * 64, yk);
+          tma_load_2d(sm + kOffV + c * kChunk128, tv, &bar[B_KVFULL], inf.g * kHeadDim + c * 64, yk);
+        }
       }
       kv_issued = it + 1;
-      StepIter si;
-      si.start(a, inf.g, inf.kg, inf.kt, inf.rk);
-      int s, h, r0;
-      uint32_t cls;
-      while (si.next(s, h, r0, cls)) {
-        const int b = steps & 1;
-        if (steps >= 2 && !wait1(&bar[B_QEMPTY + b], ((steps >> 1) - 1) & 1, a, 212)) goto abort;
-        mbar_arrive_expect_tx(&bar[B_QFULL + b], 2 * kTile64);
-        const int y = pv.segs[s].q_off + r0;
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(sm + kOffQ + b * kTile64 + c * kChunk64, tq, &bar[B_QFULL + b], h * kHeadDim + c * 64, y);
-          tma_load_2d(sm + kOffDO + b * kTile64 + c * kChunk64, tdo, &bar[B_QFULL + b], h * kHeadDim + c * 64, y);
+      for (int l = 0; l < pv.G; ++l) {
+        const int h = inf.g * pv.G + l;
+        const int hm = (pv.hm_count == 1) ? 0 : h;
+        const int n_in_list = a.list_cnt[hm * pv.RK + inf.rk];
+        const long long ebase = hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(inf.kt) * grp.pairs;
+        for (int e0 = 0; e0 < n_in_list; e0 += 32) {
+          // lane-parallel fetch of up to 32 entries and their segments
+          int2 en = make_int2(0, 0);
+          SegInfo sgl{};
+          if (e0 + lane < n_in_list) {
+            en = entries[ebase + e0 + lane];
+            sgl = pv.segs[en.x];
+          }
+          const int batch = min(32, n_in_list - e0);
+          for (int t = 0; t < batch; ++t) {
+            SegInfo sg;
+            sg.q_off = __shfl_sync(0xFFFFFFFFu, sgl.q_off, t);
+            sg.q_len = __shfl_sync(0xFFFFFFFFu, sgl.q_len, t);
+            sg.k_off = __shfl_sync(0xFFFFFFFFu, sgl.k_off, t);
+            sg.k_len = __shfl_sync(0xFFFFFFFFu, sgl.k_len, t);
+            sg.prefix = __shfl_sync(0xFFFFFFFFu, sgl.prefix, t);
+            sg.kg = 0;
+            sg.nk = 0;
+            sg.pad = 0;
+            const int ey = __shfl_sync(0xFFFFFFFFu, en.y, t);
+            const int qt = ey & 0xFFFFFF;
+            const uint32_t cls = static_cast<uint32_t>(ey >> 24) & 3u;
+            for (int half = 0; half < 2; ++half) {
+              const int r0 = qt * kTile + 64 * half;
+              if (r0 >= sg.q_len) continue;
+              const int b = steps % kRing;
+              const uint32_t reuse = steps / kRing;  // how many times ring slot b was filled before
+              if (reuse >= 1 && !waitw(&bar[B_MEMPTY + b], (reuse - 1) & 1, a, 213)) goto abort;
+              float* sl = stat_lse2(sm, b);
+              float* sd = stat_D(sm, b);
+              const size_t row0 = static_cast<size_t>(h) * pv.Tq + sg.q_off;
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                // rows past the segment end read nothing and get 0 (their tile is partial, so masked)
+                const int qi = lane + 32 * u;
+                const int i = r0 + qi;
+                const uint32_t nb = (i < sg.q_len) ? 4u : 0u;
+                const size_t src = row0 + ((i < sg.q_len) ? i : 0);
+                cp_async_4(sl + qi, a.lse2 + src, nb);
+                cp_async_4(sd + qi, a.D + src, nb);
+              }
+              cp_async_mbar_arrive_noinc(&bar[B_MFULL + b]);
+              if (cls == kTilePartial) {
+                uint32_t* sw = stat_mask(sm, b);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const int wd = lane * 8 + u;  // word = query row * 4 + key chunk
+                  sw[wd] = mask_bits(pv.mask, sg, hm, r0 + (wd >> 2), inf.kt * kTile + 32 * (wd & 3));
+                }
+              }
+              if (lane == 0) stat_meta(sm, b)->cls = static_cast<int>(cls);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&bar[B_MFULL + b]);
+              if (reuse >= 1 && !waitw(&bar[B_QEMPTY + b], (reuse - 1) & 1, a, 212)) goto abort;
+              if (lane == 0) {
+                mbar_arrive_expect_tx(&bar[B_QFULL + b], 2 * kTile64);
+                const int y = sg.q_off + r0;
+                for (int c = 0; c < 2; ++c) {
+                  tma_load_2d(sm + kOffQ + b * kTile64 + c * kChunk64, tq, &bar[B_QFULL + b], h * kHeadDim + c * 64,
+                              y);
+                  tma_load_2d(sm + kOffDO + b * kTile64 + c * kChunk64, tdo, &bar[B_QFULL + b],
+                              h * kHeadDim + c * 64, y);
+                }
+              }
+              ++steps;
+            }
+          }
         }
-        ++steps;
       }
     }
   }
 abort:
-  for (uint32_t d = 0; d < 2 && d < steps; ++d) {
-    const uint32_t idx = steps - 1 - d;
-    mbar_wait(&bar[B_QFULL + (idx & 1)], (idx >> 1) & 1, nullptr, 100000000ull, 0, 0);
+  if (lane == 0) {
+    for (uint32_t d = 0; d < kRing && d < steps; ++d) {
+      const uint32_t idx = steps - 1 - d;
+      mbar_wait(&bar[B_QFULL + idx % kRing], (idx / kRing) & 1, nullptr, 100000000ull, 0, 0);
+    }
+    if (kv_issued >= 1) mbar_wait(&bar[B_KVFULL], (kv_issued - 1) & 1, nullptr, 100000000ull, 0, 0);
   }
-  if (kv_issued >= 1) mbar_wait(&bar[B_KVFULL], (kv_issued - 1) & 1, nullptr, 100000000ull, 0, 0);
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items,
@@ -539,13 +569,13 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
       tc_fence_after();
       const int n = inf.nsteps;
       for (int p = 0; p <= n; ++p) {
-        if (p < n) {  // S^T = K Q^T, dP^T = V dO^T into TMEM buffer b
+        if (p < n) {  // S^T = K Q^T, dP^T = V dO^T into TMEM buffer b, from ring slot r
           const uint32_t idx = steps + p;
-          const int b = idx & 1;
+          const int b = idx & 1, r = idx % kRing;
           if (idx >= 2 && !wait1(&bar[B_SEMPTY + b], ((idx >> 1) - 1) & 1, a, 222)) goto abort;
-          if (!wait1(&bar[B_QFULL + b], (idx >> 1) & 1, a, 223)) goto abort;
+          if (!wait1(&bar[B_QFULL + r], (idx / kRing) & 1, a, 223)) goto abort;
           tc_fence_after();
-          const uint32_t q_addr = base + kOffQ + b * kTile64, do_addr = base + kOffDO + b * kTile64;
+          const uint32_t q_addr = base + kOffQ + r * kTile64, do_addr = base + kOffDO + r * kTile64;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t ao = (ks >> 2) * kChunk128 + (ks & 3) * 32;
@@ -565,11 +595,11 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
         }
         if (p >= 1) {  // dV += P^T dO, dK += dS^T Q for step p-1
           const uint32_t idx = steps + p - 1;
-          const int b = idx & 1;
-          if (!wait1(&bar[B_PFULL + b], (idx >> 1) & 1, a, 224)) goto abort;
+          const int r = idx % kRing;
+          if (!wait1(&bar[B_PFULL], idx & 1, a, 224)) goto abort;
           tc_fence_after();
-          const uint32_t q_addr = base + kOffQ + b * kTile64, do_addr = base + kOffDO + b * kTile64;
-          const uint32_t p_addr = base + kOffP + b * kTile64, ds_addr = base + kOffDS + b * kTile64;
+          const uint32_t q_addr = base + kOffQ + r * kTile64, do_addr = base + kOffDO + r * kTile64;
+          const uint32_t p_addr = base + kOffP, ds_addr = base + kOffDS;
           const uint32_t acc = (p > 1) ? 1u : 0u;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
@@ -581,8 +611,8 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
             umma_ss(tbase + 384, sdesc_sw128(ds_addr + ks * 32, 16, 1024),
                     sdesc_sw128(q_addr + ks * 2048, kChunk64, 1024), kIdescMN, (ks > 0) ? 1u : acc);
           }
-          umma_commit(&bar[B_PEMPTY + b]);
-          umma_commit(&bar[B_QEMPTY + b]);
+          umma_commit(&bar[B_PEMPTY]);
+          umma_commit(&bar[B_QEMPTY + r]);
           if (p == n) umma_commit(&bar[B_ACCFULL]);
         }
       }
@@ -602,7 +632,6 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   const int wq = warp & 3, half = warp >> 2;  // half: which 32 of the 64 query columns
   const int lane = threadIdx.x & 31;
   const int j = wq * 32 + lane;  // key row inside the tile = TMEM lane
-  const int ctid = threadIdx.x;  // 0..255
   const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
   const float sl2 = a.scale_log2;
   __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(a.dk);
@@ -616,33 +645,13 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
     if (!inf.valid) return;
     const KeyGroup grp = pv.kgs[inf.kg];
-    StepIter si;
-    si.start(a, inf.g, inf.kg, inf.kt, inf.rk);
-    int s, h, r0;
-    uint32_t cls;
-    while (si.next(s, h, r0, cls)) {
-      const SegInfo sg = pv.segs[s];
-      const int b = steps & 1;
-      // Stage this step's per-query statistics and, on partial tiles, the mask
-      // words in buffer b; the buffer of step p+2 is written only after every
-      // thread has passed the staging barrier of step p+1, hence done with p.
-      float* s_lse2 = reinterpret_cast<float*>(sm + kOffStat + b * kStatBytes);
-      float* s_D = s_lse2 + 64;
-      uint32_t* s_mask = reinterpret_cast<uint32_t*>(s_D + 64);  // [64 query rows][4 key chunks]
-      if (ctid < 64) {
-        const int i = r0 + ctid;
-        const size_t st = static_cast<size_t>(h) * pv.Tq + sg.q_off + i;
-        const bool ok = i < sg.q_len;
-        s_lse2[ctid] = ok ? a.lse2[st] : INFINITY;
-        s_D[ctid] = ok ? a.D[st] : 0.f;
-      }
-      if (cls == kTilePartial) {
-        const int qi = ctid >> 2, c = ctid & 3;
-        const int hm = (pv.hm_count == 1) ? 0 : h;
-        s_mask[ctid] = mask_bits(pv.mask, sg, hm, r0 + qi, inf.kt * kTile + 32 * c);
-      }
-      mbar_arrive(&bar[B_STAT]);
-      if (!waitw(&bar[B_STAT], steps & 1, a, 234)) return;
+    for (int p = 0; p < inf.nsteps; ++p, ++steps) {
+      const int b = steps & 1, r = steps % kRing;
+      if (!waitw(&bar[B_MFULL + r], (steps / kRing) & 1, a, 234)) return;
+      const float* s_lse2 = stat_lse2(sm, r);
+      const float* s_D = stat_D(sm, r);
+      const uint32_t* s_mask = stat_mask(sm, r);
+      const int cls = stat_meta(sm, r)->cls;
       if (!waitw(&bar[B_SFULL + b], (steps >> 1) & 1, a, 231)) return;
       tc_fence_after();
       float sv[32], dp[32];
@@ -662,7 +671,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
           const uint32_t w = s_mask[(32 * half + k) * 4 + wq];
-          if (!((w >> lane) & 1u)) sv[k] = -INFINITY;
+          sv[k] = ((w >> lane) & 1u) ? sv[k] : -INFINITY;
         }
       }
       uint32_t pp[16], pd[16];
@@ -674,11 +683,14 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         pp[k] = pack_bf16x2(p0, p1);
         pd[k] = pack_bf16x2(p0 * (dp[2 * k] - s_D[q0]), p1 * (dp[2 * k + 1] - s_D[q0 + 1]));
       }
-      if (steps >= 2 && !waitw(&bar[B_PEMPTY + b], ((steps >> 1) - 1) & 1, a, 232)) return;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_MEMPTY + r]);  // done with this step's staged data
+      // the previous step's dV/dK products have read P^T and dS^T
+      if (steps >= 1 && !waitw(&bar[B_PEMPTY], (steps - 1) & 1, a, 232)) return;
       // P^T and dS^T rows: [128 keys x 64 queries], K-major, one 128-byte swizzle chunk;
       // this thread writes the 4 x 16-byte pieces of its 32 query columns.
-      uint8_t* pbuf = sm + kOffP + b * kTile64;
-      uint8_t* dbuf = sm + kOffDS + b * kTile64;
+      uint8_t* pbuf = sm + kOffP;
+      uint8_t* dbuf = sm + kOffDS;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int piece = 4 * half + u;
@@ -687,8 +699,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bar[B_PFULL + b]);
-      ++steps;
+      mbar_arrive(&bar[B_PFULL]);
     }
     // epilogue: rows of the key group only
     const int jg = inf.kt * kTile + j;
@@ -746,13 +757,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
-    mbar_init(&bar[B_SEMPTY], 256);
-    mbar_init(&bar[B_SEMPTY1], 256);
+    for (int b = 0; b < 2; ++b) mbar_init(&bar[B_SEMPTY + b], 256);
     mbar_init(&bar[B_PFULL], 256);
-    mbar_init(&bar[B_PFULL1], 256);
-    mbar_init(&bar[B_STAT], 256);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&bar[B_MEMPTY + r], 8);
+      mbar_init(&bar[B_MFULL + r], 33);  // 32 cp.async completions + the producer's own arrive
+    }
     mbar_init(&bar[B_ITEMPTY], 9);
-    mbar_init(&bar[B_ITEMPTY1], 9);
+    mbar_init(&bar[B_ITEMPTY + 1], 9);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -760,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   if (warp == 9) {
-    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
+    producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
   } else if (warp == 8) {
     if (lane == 0) mma_issuer(a, sm, bar, items, tbase);
   } else {

@@ -182,9 +182,11 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
       tc_fence_after();
       const int n = inf.cnt;
       bool first_pv[2] = {true, true};
+      uint32_t e_cur = (n > 0) ? entries[inf.ebase] : 0u, e_prev = 0u;
       for (int t = 0; t <= n; ++t) {
+        const uint32_t e_nxt = (t + 1 < n) ? entries[inf.ebase + t + 1] : 0u;
         if (t < n) {  // S_x(t) = Q_x K(t)^T
-          const uint32_t e = entries[inf.ebase + t];
+          const uint32_t e = e_cur;
           const uint32_t idx = kv_iter + k_load_index(t);
           const int stg = idx % kStages;
           if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 22)) goto abort;
@@ -209,7 +211,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
         }
         if (t >= 1) {  // O_x += P_x(t-1) V(t-1)
           const int u = t - 1;
-          const uint32_t e = entries[inf.ebase + u];
+          const uint32_t e = e_prev;
           const uint32_t idx = kv_iter + v_load_index(u, n);
           const int stg = idx % kStages;
           if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 24)) goto abort;
@@ -233,6 +235,8 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
           }
           umma_commit(&bar[B_KVEMPTY + stg]);
         }
+        e_prev = e_cur;
+        e_cur = e_nxt;
       }
       if (n == 0) umma_commit(&bar[B_QEMPTY]);
       kv_iter += 2 * n;
@@ -270,8 +274,10 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
     const bool valid = i < sg.q_len;
     float m_use = -INFINITY, l = 0.f;
     bool any = false;
+    uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
     for (int t = 0; t < inf.cnt; ++t) {
-      const uint32_t e = entries[inf.ebase + t];
+      const uint32_t e = e_next;  // the next entry's load overlaps this tile's work
+      if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
       const uint32_t cls = (e >> (24 + 2 * x)) & 3u;
       if (cls == kTileEmpty) continue;
       const int kt = static_cast<int>(e & 0xFFFFFFu);
@@ -294,8 +300,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
         for (int c = 0; c < 4; ++c) {
           const uint32_t bits = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (!((bits >> k) & 1u)) s[32 * c + k] = -INFINITY;
+          for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
         }
       }
       float mx = -INFINITY;
@@ -311,6 +316,8 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
         need = true;
         m_use = m_new;
       }
+      // P = exp2(s*scale*log2e - m) in bf16; computed before waiting for the
+      // previous PV so that the score registers are free during the wait
       const float base = (m_use == -INFINITY) ? 0.f : m_use;
       float sum = 0.f;
       uint32_t pk[64];

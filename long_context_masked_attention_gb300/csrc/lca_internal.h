@@ -50,7 +50,7 @@ void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int
                              size_t keep_bytes, int* status, cudaStream_t st);
 void launch_plan_fwd(const PlanView& pv, const WorkList& wl, cudaStream_t st);
 void launch_plan_dq(const PlanView& pv, const WorkList& wl, cudaStream_t st);
-void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, cudaStream_t st);
+void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, int* list_steps, cudaStream_t st);
 void launch_sort(const WorkList& wl, cudaStream_t st);
 void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st);
 void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st);
@@ -66,7 +66,8 @@ struct AttnArgs {
   const int* cnt;
   const int* order;
   const void* entries;
-  const int* list_cnt;  // dK/dV: entries per (map head, key tile) list
+  const int* list_cnt;    // dK/dV: entries per (map head, key tile) list
+  const int* list_steps;  // dK/dV: 64-row query steps per list
   int* counter;
   int n_work;
   int expand;

@@ -117,7 +117,8 @@ void launch_plan_dq(const PlanView& pv, const WorkList& wl, cudaStream_t st) {
 // (H' = 1) the unit has one list; for per-head maps it has one list per query
 // head of the KV head.  Entry = {segment, query tile | class << 24}.
 __global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* __restrict__ list_cnt,
-                                     int2* __restrict__ entries, uint32_t* __restrict__ hist, int n_units) {
+                                     int* __restrict__ list_steps, int2* __restrict__ entries,
+                                     uint32_t* __restrict__ hist, int n_units) {
   const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= n_units) return;
@@ -130,7 +131,7 @@ __global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* _
   for (int l = 0; l < nlists; ++l) {
     const int hm = (pv.hm_count == 1) ? 0 : gm * pv.G + l;
     int2* out = entries + hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(kt) * grp.pairs;
-    int n = 0;
+    int n = 0, steps = 0;
     for (int si = grp.seg_begin; si < grp.seg_end; ++si) {
       const int s = pv.kg_segs[si];
       const SegInfo sg = pv.segs[s];
@@ -141,10 +142,14 @@ __global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* _
         if (c) {
           if (lane == 0) out[n] = make_int2(s, qt | static_cast<int>(c << 24));
           ++n;
+          steps += (qt * kTile + 64 < sg.q_len) ? 2 : 1;  // 64-row halves inside the segment
         }
       }
     }
-    if (lane == 0) list_cnt[hm * pv.RK + rk] = n;
+    if (lane == 0) {
+      list_cnt[hm * pv.RK + rk] = n;
+      list_steps[hm * pv.RK + rk] = steps;
+    }
     cost += n;
   }
   if (lane == 0) {
@@ -153,12 +158,12 @@ __global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* _
   }
 }
 
-void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, cudaStream_t st) {
+void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, int* list_steps, cudaStream_t st) {
   const int n_units = wl.n_sorted;
   if (n_units == 0) return;
   note_launches(1);
-  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, wl.cnt, list_cnt, static_cast<int2*>(wl.entries),
-                                                          wl.hist, n_units);
+  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, wl.cnt, list_cnt, list_steps,
+                                                          static_cast<int2*>(wl.entries), wl.hist, n_units);
 }
 
 // ---------------------------------------------------------------- cost sort
