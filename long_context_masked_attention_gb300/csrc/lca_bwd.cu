@@ -56,17 +56,22 @@ __device__ __forceinline__ uint4 pack8(const float* v, float mul) {
 // ====================================================================== dQ
 namespace dq {
 
+// Shared memory: Q and dO tiles of the item, a 3-slot K ring and a 2-slot V
+// ring.  TMEM: S [0,128), dP [128,256), dQ [256,384), and dS as bf16 in two
+// 64-column buffers [384,448), [448,512) that the dQ product reads directly.
+constexpr int kKRing = 3, kVRing = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kOffQ + kTile128;
-constexpr int kOffDS = kOffDO + kTile128;
-constexpr int kOffK = kOffDS + kTile128;  // 2-slot K ring
-constexpr int kOffV = kOffK + 2 * kTile128;  // 2-slot V ring
-constexpr int kOffCtl = kOffV + 2 * kTile128;
+constexpr int kOffK = kOffDO + kTile128;
+constexpr int kOffV = kOffK + kKRing * kTile128;
+constexpr int kOffCtl = kOffV + kVRing * kTile128;
 constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
 
 enum : int {
-  B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1, B_VEMPTY, B_VEMPTY1,
-  B_SFULL, B_SEMPTY, B_DSFULL, B_DSEMPTY, B_DQFULL, B_ITFULL, B_ITFULL1, B_ITEMPTY, B_ITEMPTY1, B_DRAIN, B_COUNT
+  B_QFULL = 0, B_QEMPTY,
+  B_KFULL, B_KEMPTY = B_KFULL + kKRing, B_VFULL = B_KEMPTY + kKRing, B_VEMPTY = B_VFULL + kVRing,
+  B_SFULL = B_VEMPTY + kVRing, B_SEMPTY, B_DSFULL, B_DSEMPTY = B_DSFULL + 2, B_DQFULL = B_DSEMPTY + 2,
+  B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_DRAIN = B_ITEMPTY + 2, B_COUNT
 };
 
 struct Item {
@@ -79,7 +84,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                                          Item* items) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
-  uint32_t tiles = 0;  // key tiles loaded so far (K and V rings advance together)
+  uint32_t tiles = 0;  // key tiles loaded so far
   uint32_t k_issued = 0, v_issued = 0;
   int q_issued = 0;
   int it = 0;
@@ -115,32 +120,34 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       }
       q_issued = it + 1;
       const int g = inf.head / pv.G;
+      uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
       for (int t = 0; t < inf.cnt; ++t, ++tiles) {
-        const int kt = static_cast<int>(entries[inf.ebase + t] & 0xFFFFFFu);
+        const uint32_t e = e_next;
+        if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
+        const int kt = static_cast<int>(e & 0xFFFFFFu);
         const int yk = sg.k_off + kt * kTile;
-        const int b = tiles & 1;
-        const uint32_t ph = ((tiles >> 1) - 1) & 1;
-        if (tiles >= 2 && !wait1(&bar[B_KEMPTY + b], ph, a, 112)) goto abort;
-        mbar_arrive_expect_tx(&bar[B_KFULL + b], kTile128);
-        tma_load_2d(sm + kOffK + b * kTile128, tk, &bar[B_KFULL + b], g * kHeadDim, yk);
-        tma_load_2d(sm + kOffK + b * kTile128 + kChunk128, tk, &bar[B_KFULL + b], g * kHeadDim + 64, yk);
+        const int kr = tiles % kKRing, vr = tiles % kVRing;
+        if (tiles >= kKRing && !wait1(&bar[B_KEMPTY + kr], ((tiles / kKRing) - 1) & 1, a, 112)) goto abort;
+        mbar_arrive_expect_tx(&bar[B_KFULL + kr], kTile128);
+        tma_load_2d(sm + kOffK + kr * kTile128, tk, &bar[B_KFULL + kr], g * kHeadDim, yk);
+        tma_load_2d(sm + kOffK + kr * kTile128 + kChunk128, tk, &bar[B_KFULL + kr], g * kHeadDim + 64, yk);
         k_issued = tiles + 1;
-        if (tiles >= 2 && !wait1(&bar[B_VEMPTY + b], ph, a, 113)) goto abort;
-        mbar_arrive_expect_tx(&bar[B_VFULL + b], kTile128);
-        tma_load_2d(sm + kOffV + b * kTile128, tv, &bar[B_VFULL + b], g * kHeadDim, yk);
-        tma_load_2d(sm + kOffV + b * kTile128 + kChunk128, tv, &bar[B_VFULL + b], g * kHeadDim + 64, yk);
+        if (tiles >= kVRing && !wait1(&bar[B_VEMPTY + vr], ((tiles / kVRing) - 1) & 1, a, 113)) goto abort;
+        mbar_arrive_expect_tx(&bar[B_VFULL + vr], kTile128);
+        tma_load_2d(sm + kOffV + vr * kTile128, tv, &bar[B_VFULL + vr], g * kHeadDim, yk);
+        tma_load_2d(sm + kOffV + vr * kTile128 + kChunk128, tv, &bar[B_VFULL + vr], g * kHeadDim + 64, yk);
         v_issued = tiles + 1;
       }
     }
   }
 abort:
-  for (uint32_t d = 0; d < 2 && d < k_issued; ++d) {
+  for (uint32_t d = 0; d < kKRing && d < k_issued; ++d) {
     const uint32_t idx = k_issued - 1 - d;
-    mbar_wait(&bar[B_KFULL + (idx & 1)], (idx >> 1) & 1, nullptr, 100000000ull, 0, 0);
+    mbar_wait(&bar[B_KFULL + idx % kKRing], (idx / kKRing) & 1, nullptr, 100000000ull, 0, 0);
   }
-  for (uint32_t d = 0; d < 2 && d < v_issued; ++d) {
+  for (uint32_t d = 0; d < kVRing && d < v_issued; ++d) {
     const uint32_t idx = v_issued - 1 - d;
-    mbar_wait(&bar[B_VFULL + (idx & 1)], (idx >> 1) & 1, nullptr, 100000000ull, 0, 0);
+    mbar_wait(&bar[B_VFULL + idx % kVRing], (idx / kVRing) & 1, nullptr, 100000000ull, 0, 0);
   }
   if (q_issued >= 1) mbar_wait(&bar[B_QFULL], (q_issued - 1) & 1, nullptr, 100000000ull, 0, 0);
 }
@@ -148,10 +155,9 @@ abort:
 __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items,
                                            uint32_t tbase) {
   const uint32_t base = smem_u32(sm);
-  const uint32_t q_addr = base + kOffQ, do_addr = base + kOffDO, ds_addr = base + kOffDS;
-  uint32_t tiles = 0;     // key tiles consumed (ring position)
-  uint32_t sdp = 0;       // S/dP products issued (TMEM reuse count)
-  uint32_t dsn = 0;       // dQ products issued (dS buffer reuse count)
+  const uint32_t q_addr = base + kOffQ, do_addr = base + kOffDO;
+  uint32_t tiles = 0;  // key tiles consumed (ring positions, dS buffers)
+  uint32_t sdp = 0;    // S/dP products issued (TMEM reuse count)
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 120)) goto abort;
@@ -165,21 +171,20 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
       for (int t = 0; t <= n; ++t) {
         if (t < n) {  // S = Q K^T, dP = dO V^T for key tile t
           const uint32_t idx = tiles + t;
-          const int b = idx & 1;
-          const uint32_t ph = (idx >> 1) & 1;
+          const int kr = idx % kKRing, vr = idx % kVRing;
           if (sdp >= 1 && !wait1(&bar[B_SEMPTY], (sdp - 1) & 1, a, 122)) goto abort;
-          if (!wait1(&bar[B_KFULL + b], ph, a, 123)) goto abort;
+          if (!wait1(&bar[B_KFULL + kr], (idx / kKRing) & 1, a, 123)) goto abort;
           tc_fence_after();
-          const uint32_t k_addr = base + kOffK + b * kTile128;
+          const uint32_t k_addr = base + kOffK + kr * kTile128;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
             umma_ss(tbase + 0, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdesc128,
                     ks > 0);
           }
-          if (!wait1(&bar[B_VFULL + b], ph, a, 124)) goto abort;
+          if (!wait1(&bar[B_VFULL + vr], (idx / kVRing) & 1, a, 124)) goto abort;
           tc_fence_after();
-          const uint32_t v_addr = base + kOffV + b * kTile128;
+          const uint32_t v_addr = base + kOffV + vr * kTile128;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
@@ -187,25 +192,23 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
                     kIdesc128, ks > 0);
           }
           umma_commit(&bar[B_SFULL]);
-          umma_commit(&bar[B_VEMPTY + b]);
+          umma_commit(&bar[B_VEMPTY + vr]);
           ++sdp;
           if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
         }
-        if (t >= 1) {  // dQ += dS K for key tile t-1
+        if (t >= 1) {  // dQ += dS K for key tile t-1, dS read from TMEM
           const uint32_t idx = tiles + t - 1;
-          const int b = idx & 1;
-          if (!wait1(&bar[B_DSFULL], dsn & 1, a, 125)) goto abort;
+          const int db = idx & 1, kr = idx % kKRing;
+          if (!wait1(&bar[B_DSFULL + db], (idx >> 1) & 1, a, 125)) goto abort;
           tc_fence_after();
-          const uint32_t k_addr = base + kOffK + b * kTile128;
+          const uint32_t k_addr = base + kOffK + kr * kTile128;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t aoff = (ks >> 2) * kChunk128 + (ks & 3) * 32;
-            umma_ss(tbase + 256, sdesc_sw128(ds_addr + aoff, 16, 1024),
-                    sdesc_sw128(k_addr + ks * 2048, kChunk128, 1024), kIdescMN, (ks > 0 || t > 1) ? 1u : 0u);
+            umma_ts(tbase + 256, tbase + 384 + 64 * db + 8 * ks, sdesc_sw128(k_addr + ks * 2048, kChunk128, 1024),
+                    kIdescMN, (ks > 0 || t > 1) ? 1u : 0u);
           }
-          umma_commit(&bar[B_DSEMPTY]);
-          umma_commit(&bar[B_KEMPTY + b]);
-          ++dsn;
+          umma_commit(&bar[B_DSEMPTY + db]);
+          umma_commit(&bar[B_KEMPTY + kr]);
           if (t == n) umma_commit(&bar[B_DQFULL]);
         }
       }
@@ -227,9 +230,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   const int row = wq * 32 + lane;
   const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
   const float sl2 = a.scale_log2;
-  uint8_t* sDS = sm + kOffDS + half * kChunk128;  // this thread's 64 key columns = one swizzle chunk
   __nv_bfloat16* dQ = static_cast<__nv_bfloat16*>(a.dq);
-  uint32_t sdp = 0, dsn = 0, items_done = 0;
+  uint32_t tiles = 0, sdp = 0, items_done = 0;
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 130)) return;
@@ -244,7 +246,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     const float lse2 = valid ? a.lse2[stat] : INFINITY;
     const float Dv = valid ? a.D[stat] : 0.f;
     uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
-    for (int t = 0; t < inf.cnt; ++t) {
+    for (int t = 0; t < inf.cnt; ++t, ++tiles) {
       const uint32_t e = e_next;  // the next entry's load overlaps this tile's work
       if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
       const uint32_t cls = (e >> 24) & 3u;
@@ -281,15 +283,14 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, -lse2));
         pk[k] = pack_bf16x2(p0 * (dp[2 * k] - Dv), p1 * (dp[2 * k + 1] - Dv));
       }
-      if (dsn >= 1 && !waitw(&bar[B_DSEMPTY], (dsn - 1) & 1, a, 132)) return;
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 v = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        *reinterpret_cast<uint4*>(sDS + row * 128 + ((u ^ (row & 7)) << 4)) = v;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bar[B_DSFULL]);
-      ++dsn;
+      // dS (bf16) into TMEM buffer db, this thread's 64 key columns = 32 packed columns
+      const int db = tiles & 1;
+      if (tiles >= 2 && !waitw(&bar[B_DSEMPTY + db], ((tiles >> 1) - 1) & 1, a, 132)) return;
+      tc_fence_after();
+      tmem_st32(tbase + tl + 384 + 64 * db + 32 * half, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[B_DSFULL + db]);
     }
     __nv_bfloat16* qrow = dQ + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + inf.head) * kHeadDim +
                           half * 64;
@@ -335,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
     mbar_init(&bar[B_SEMPTY], 256);
     mbar_init(&bar[B_DSFULL], 256);
+    mbar_init(&bar[B_DSFULL + 1], 256);
     mbar_init(&bar[B_ITEMPTY], 9);
-    mbar_init(&bar[B_ITEMPTY1], 9);
+    mbar_init(&bar[B_ITEMPTY + 1], 9);
     fence_mbar_init();
   }
   tc_fence_before();
