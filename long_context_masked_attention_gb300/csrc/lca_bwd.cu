@@ -155,7 +155,12 @@ abort:
 __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items,
                                            uint32_t tbase) {
   const uint32_t base = smem_u32(sm);
-  const uint32_t q_addr = base + kOffQ, do_addr = base + kOffDO;
+  // operand descriptors built once; every MMA below only adds a byte offset
+  const uint64_t dQd = sdesc_sw128(base + kOffQ, 16, 1024);
+  const uint64_t dOd = sdesc_sw128(base + kOffDO, 16, 1024);
+  const uint64_t dKk = sdesc_sw128(base + kOffK, 16, 1024);         // K ring, K-major
+  const uint64_t dKn = sdesc_sw128(base + kOffK, kChunk128, 1024);  // K ring, N-major
+  const uint64_t dVk = sdesc_sw128(base + kOffV, 16, 1024);
   uint32_t tiles = 0;  // key tiles consumed (ring positions, dS buffers)
   uint32_t sdp = 0;    // S/dP products issued (TMEM reuse count)
   for (int it = 0;; ++it) {
@@ -175,21 +180,19 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           if (sdp >= 1 && !wait1(&bar[B_SEMPTY], (sdp - 1) & 1, a, 122)) goto abort;
           if (!wait1(&bar[B_KFULL + kr], (idx / kKRing) & 1, a, 123)) goto abort;
           tc_fence_after();
-          const uint32_t k_addr = base + kOffK + kr * kTile128;
+          const uint64_t dK = desc_add(dKk, kr * kTile128);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
-            umma_ss(tbase + 0, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024), kIdesc128,
-                    ks > 0);
+            umma_ss(tbase + 0, desc_add(dQd, off), desc_add(dK, off), kIdesc128, ks > 0);
           }
           if (!wait1(&bar[B_VFULL + vr], (idx / kVRing) & 1, a, 124)) goto abort;
           tc_fence_after();
-          const uint32_t v_addr = base + kOffV + vr * kTile128;
+          const uint64_t dV = desc_add(dVk, vr * kTile128);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
-            umma_ss(tbase + 128, sdesc_sw128(do_addr + off, 16, 1024), sdesc_sw128(v_addr + off, 16, 1024),
-                    kIdesc128, ks > 0);
+            umma_ss(tbase + 128, desc_add(dOd, off), desc_add(dV, off), kIdesc128, ks > 0);
           }
           umma_commit(&bar[B_SFULL]);
           umma_commit(&bar[B_VEMPTY + vr]);
@@ -201,11 +204,12 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           const int db = idx & 1, kr = idx % kKRing;
           if (!wait1(&bar[B_DSFULL + db], (idx >> 1) & 1, a, 125)) goto abort;
           tc_fence_after();
-          const uint32_t k_addr = base + kOffK + kr * kTile128;
+          const uint64_t dK = desc_add(dKn, kr * kTile128);
+          const uint32_t tA = tbase + 384 + 64 * db;
+          const uint32_t acc0 = (t > 1) ? 1u : 0u;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            umma_ts(tbase + 256, tbase + 384 + 64 * db + 8 * ks, sdesc_sw128(k_addr + ks * 2048, kChunk128, 1024),
-                    kIdescMN, (ks > 0 || t > 1) ? 1u : 0u);
+            umma_ts(tbase + 256, tA + 8 * ks, desc_add(dK, ks * 2048), kIdescMN, ks > 0 ? 1u : acc0);
           }
           umma_commit(&bar[B_DSEMPTY + db]);
           umma_commit(&bar[B_KEMPTY + kr]);
@@ -266,7 +270,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bar[B_SEMPTY]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_SEMPTY]);
       ++sdp;
       if (cls == kTilePartial) {
 #pragma unroll
@@ -290,7 +295,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       tmem_st32(tbase + tl + 384 + 64 * db + 32 * half, pk);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[B_DSFULL + db]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_DSFULL + db]);
     }
     __nv_bfloat16* qrow = dQ + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + inf.head) * kHeadDim +
                           half * 64;
@@ -334,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
-    mbar_init(&bar[B_SEMPTY], 256);
-    mbar_init(&bar[B_DSFULL], 256);
-    mbar_init(&bar[B_DSFULL + 1], 256);
+    mbar_init(&bar[B_SEMPTY], 8);  // one arrival per compute warp
+    mbar_init(&bar[B_DSFULL], 8);
+    mbar_init(&bar[B_DSFULL + 1], 8);
     mbar_init(&bar[B_ITEMPTY], 9);
     mbar_init(&bar[B_ITEMPTY + 1], 9);
     fence_mbar_init();
@@ -557,7 +563,15 @@ abort:
 __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items,
                                            uint32_t tbase) {
   const uint32_t base = smem_u32(sm);
-  const uint32_t k_addr = base + kOffK, v_addr = base + kOffV;
+  // operand descriptors built once; every MMA below only adds a byte offset
+  const uint64_t dKk = sdesc_sw128(base + kOffK, 16, 1024);
+  const uint64_t dVk = sdesc_sw128(base + kOffV, 16, 1024);
+  const uint64_t dQk = sdesc_sw128(base + kOffQ, 16, 1024);         // Q ring, K-major (B of S^T)
+  const uint64_t dOk = sdesc_sw128(base + kOffDO, 16, 1024);        // dO ring, K-major (B of dP^T)
+  const uint64_t dQn = sdesc_sw128(base + kOffQ, kChunk64, 1024);   // Q ring, N-major (B of dK)
+  const uint64_t dOn = sdesc_sw128(base + kOffDO, kChunk64, 1024);  // dO ring, N-major (B of dV)
+  const uint64_t dPk = sdesc_sw128(base + kOffP, 16, 1024);
+  const uint64_t dSk = sdesc_sw128(base + kOffDS, 16, 1024);
   uint32_t steps = 0;  // global step counter (rings and TMEM double buffers)
   int acc_items = 0;
   for (int it = 0;; ++it) {
@@ -577,20 +591,19 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           if (idx >= 2 && !wait1(&bar[B_SEMPTY + b], ((idx >> 1) - 1) & 1, a, 222)) goto abort;
           if (!wait1(&bar[B_QFULL + r], (idx / kRing) & 1, a, 223)) goto abort;
           tc_fence_after();
-          const uint32_t q_addr = base + kOffQ + r * kTile64, do_addr = base + kOffDO + r * kTile64;
+          const uint64_t dQ = desc_add(dQk, r * kTile64), dO = desc_add(dOk, r * kTile64);
+          const uint32_t tS = tbase + 64 * b, tP = tbase + 128 + 64 * b;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t ao = (ks >> 2) * kChunk128 + (ks & 3) * 32;
             const uint32_t bo = (ks >> 2) * kChunk64 + (ks & 3) * 32;
-            umma_ss(tbase + 64 * b, sdesc_sw128(k_addr + ao, 16, 1024), sdesc_sw128(q_addr + bo, 16, 1024), kIdesc64,
-                    ks > 0);
+            umma_ss(tS, desc_add(dKk, ao), desc_add(dQ, bo), kIdesc64, ks > 0);
           }
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t ao = (ks >> 2) * kChunk128 + (ks & 3) * 32;
             const uint32_t bo = (ks >> 2) * kChunk64 + (ks & 3) * 32;
-            umma_ss(tbase + 128 + 64 * b, sdesc_sw128(v_addr + ao, 16, 1024), sdesc_sw128(do_addr + bo, 16, 1024),
-                    kIdesc64, ks > 0);
+            umma_ss(tP, desc_add(dVk, ao), desc_add(dO, bo), kIdesc64, ks > 0);
           }
           umma_commit(&bar[B_SFULL + b]);
           if (p == n - 1) umma_commit(&bar[B_KVEMPTY]);
@@ -600,19 +613,14 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           const int r = idx % kRing;
           if (!wait1(&bar[B_PFULL], idx & 1, a, 224)) goto abort;
           tc_fence_after();
-          const uint32_t q_addr = base + kOffQ + r * kTile64, do_addr = base + kOffDO + r * kTile64;
-          const uint32_t p_addr = base + kOffP, ds_addr = base + kOffDS;
+          const uint64_t dQ = desc_add(dQn, r * kTile64), dO = desc_add(dOn, r * kTile64);
           const uint32_t acc = (p > 1) ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            umma_ss(tbase + 256, sdesc_sw128(p_addr + ks * 32, 16, 1024),
-                    sdesc_sw128(do_addr + ks * 2048, kChunk64, 1024), kIdescMN, (ks > 0) ? 1u : acc);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            umma_ss(tbase + 256, desc_add(dPk, ks * 32), desc_add(dO, ks * 2048), kIdescMN, (ks > 0) ? 1u : acc);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            umma_ss(tbase + 384, sdesc_sw128(ds_addr + ks * 32, 16, 1024),
-                    sdesc_sw128(q_addr + ks * 2048, kChunk64, 1024), kIdescMN, (ks > 0) ? 1u : acc);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            umma_ss(tbase + 384, desc_add(dSk, ks * 32), desc_add(dQ, ks * 2048), kIdescMN, (ks > 0) ? 1u : acc);
           umma_commit(&bar[B_PEMPTY]);
           umma_commit(&bar[B_QEMPTY + r]);
           if (p == n) umma_commit(&bar[B_ACCFULL]);
@@ -668,7 +676,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bar[B_SEMPTY + b]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_SEMPTY + b]);
       if (cls == kTilePartial) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
@@ -701,7 +710,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(&bar[B_PFULL]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_PFULL]);
     }
     // epilogue: rows of the key group only
     const int jg = inf.kt * kTile + j;
@@ -759,8 +769,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
-    for (int b = 0; b < 2; ++b) mbar_init(&bar[B_SEMPTY + b], 256);
-    mbar_init(&bar[B_PFULL], 256);
+    for (int b = 0; b < 2; ++b) mbar_init(&bar[B_SEMPTY + b], 8);  // one arrival per compute warp
+    mbar_init(&bar[B_PFULL], 8);
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&bar[B_MEMPTY + r], 8);
       mbar_init(&bar[B_MFULL + r], 33);  // 32 cp.async completions + the producer's own arrive

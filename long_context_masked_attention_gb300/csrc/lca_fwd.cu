@@ -168,7 +168,11 @@ abort:
 __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8_t* sKV, uint8_t* sP, uint64_t* bar,
                                            Item* items, uint32_t tbase) {
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
-  const uint32_t q_addr = smem_u32(sQ), kv_addr = smem_u32(sKV), p_addr = smem_u32(sP);
+  // operand descriptors built once; every MMA below only adds a byte offset
+  const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);           // Q_x, K-major
+  const uint64_t dK0 = sdesc_sw128(smem_u32(sKV), 16, 1024);          // K tile, K-major
+  const uint64_t dV0 = sdesc_sw128(smem_u32(sKV), kChunkBytes, 1024); // V tile, N-major
+  const uint64_t dP0 = sdesc_sw128(smem_u32(sP), 16, 1024);           // P_x, K-major
   uint32_t kv_iter = 0;
   uint32_t s_iss[2] = {0, 0}, p_iss[2] = {0, 0};
   for (int it = 0;; ++it) {
@@ -191,17 +195,18 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
           const int stg = idx % kStages;
           if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 22)) goto abort;
           tc_fence_after();
-          const uint32_t k_addr = kv_addr + stg * kTileBytes;
+          const uint64_t dK = desc_add(dK0, stg * kTileBytes);
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (((e >> (24 + 2 * x)) & 3u) == 0) continue;
             if (s_iss[x] >= 1 && !wait1(&bar[B_SEMPTY + x], (s_iss[x] - 1) & 1, a, 23)) goto abort;
             tc_fence_after();
+            const uint64_t dQx = desc_add(dQ0, x * kTileBytes);
+            const uint32_t tS = tbase + 128 * x;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t koff = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
-              umma_ss(tbase + 128 * x, sdesc_sw128(q_addr + x * kTileBytes + koff, 16, 1024),
-                      sdesc_sw128(k_addr + koff, 16, 1024), kIdescS, ks > 0 ? 1u : 0u);
+              umma_ss(tS, desc_add(dQx, koff), desc_add(dK, koff), kIdescS, ks > 0 ? 1u : 0u);
             }
             umma_commit(&bar[B_SFULL + x]);
             ++s_iss[x];
@@ -216,18 +221,19 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
           const int stg = idx % kStages;
           if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 24)) goto abort;
           tc_fence_after();
-          const uint32_t v_addr = kv_addr + stg * kTileBytes;
+          const uint64_t dV = desc_add(dV0, stg * kTileBytes);
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (((e >> (24 + 2 * x)) & 3u) == 0) continue;
             if (!wait1(&bar[B_PFULL + x], p_iss[x] & 1, a, 25)) goto abort;
             tc_fence_after();
+            const uint64_t dPx = desc_add(dP0, x * kTileBytes);
+            const uint32_t tO = tbase + 256 + 128 * x;
+            const uint32_t acc0 = first_pv[x] ? 0u : 1u;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t poff = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
-              umma_ss(tbase + 256 + 128 * x, sdesc_sw128(p_addr + x * kTileBytes + poff, 16, 1024),
-                      sdesc_sw128(v_addr + ks * 2048, kChunkBytes, 1024), kIdescO,
-                      (ks > 0 || !first_pv[x]) ? 1u : 0u);
+              umma_ss(tO, desc_add(dPx, poff), desc_add(dV, ks * 2048), kIdescO, ks > 0 ? 1u : acc0);
             }
             first_pv[x] = false;
             umma_commit(&bar[B_OFULL + x]);
@@ -293,7 +299,8 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
       }
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(&bar[B_SEMPTY + x]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_SEMPTY + x]);
       ++s_cons;
       if (cls == kTilePartial) {
 #pragma unroll
@@ -357,7 +364,8 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
         }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bar[B_PFULL + x]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_PFULL + x]);
       ++p_prod;
       any = true;
     }
@@ -423,8 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bar[B_SFULL + x], 1);
-      mbar_init(&bar[B_SEMPTY + x], 128);
-      mbar_init(&bar[B_PFULL + x], 128);
+      mbar_init(&bar[B_SEMPTY + x], 4);  // one arrival per softmax warp
+      mbar_init(&bar[B_PFULL + x], 4);
       mbar_init(&bar[B_OFULL + x], 1);
       mbar_init(&bar[B_ITFULL + x], 1);
       mbar_init(&bar[B_ITEMPTY + x], 9);

@@ -216,6 +216,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// Descriptor of the same operand moved by `byte_off` bytes (a multiple of 16):
+// only the 14-bit start-address field in the low word changes, and shared
+// memory addresses stay below 2^18, so one 32-bit add suffices.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) {
+  const uint32_t lo = static_cast<uint32_t>(d) + (byte_off >> 4);
+  return (static_cast<uint64_t>(static_cast<uint32_t>(d >> 32)) << 32) | lo;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and f32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4)                                   // D format: f32
