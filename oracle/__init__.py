@@ -24,6 +24,8 @@ from .attention import (  # noqa: F401
     attention_forward,
     attention_backward,
     forward_rows,
+    backward_rows,
+    key_grads_from_rows,
     segment_head_forward,
     segment_head_backward,
 )

@@ -117,3 +117,40 @@ def forward_rows(prob, q, k, v, seg_index, head, rows):
     mask = segment_mask(prob.mask, seg_index, seg, head, rows)
     o, lse, _ = segment_head_forward(qr, kk, vv, mask, scale)
     return o, lse
+
+
+def backward_rows(prob, q, k, v, do, seg_index, head, rows):
+    """dQ for selected rows (segment-relative) of one segment and head: a
+    row's softmax, D_i and dS_ij depend on that row alone."""
+    seg = prob.segments[seg_index]
+    g = _kv_head(prob, head)
+    scale = prob.softmax_scale
+    rows = np.asarray(rows)
+    qr = _f64(q[seg.q_off + rows, head])
+    dor = _f64(do[seg.q_off + rows, head])
+    kk = _f64(k[seg.k_off:seg.k_off + seg.k_len, g])
+    vv = _f64(v[seg.k_off:seg.k_off + seg.k_len, g])
+    mask = segment_mask(prob.mask, seg_index, seg, head, rows)
+    dq, _, _, _, _, _ = segment_head_backward(qr, kk, vv, dor, mask, scale)
+    return dq
+
+
+def key_grads_from_rows(prob, q, k, v, do, seg_index, head, rows, key_cols):
+    """Contribution of the given query rows of one segment and head to dK and
+    dV of the given key columns (segment-relative): dK_j = tau sum_i dS_ij q_i,
+    dV_j = sum_i P_ij dO_i over the listed rows only."""
+    seg = prob.segments[seg_index]
+    g = _kv_head(prob, head)
+    scale = prob.softmax_scale
+    rows = np.asarray(rows)
+    key_cols = np.asarray(key_cols)
+    qr = _f64(q[seg.q_off + rows, head])
+    dor = _f64(do[seg.q_off + rows, head])
+    kk = _f64(k[seg.k_off:seg.k_off + seg.k_len, g])
+    vv = _f64(v[seg.k_off:seg.k_off + seg.k_len, g])
+    mask = segment_mask(prob.mask, seg_index, seg, head, rows)
+    _, _, p = segment_head_forward(qr, kk, vv, mask, scale)
+    dp = dor @ vv.T
+    D = (p * dp).sum(axis=1)
+    ds = p * (dp - D[:, None])
+    return scale * (ds[:, key_cols].T @ qr), p[:, key_cols].T @ dor

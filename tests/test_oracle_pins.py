@@ -340,3 +340,36 @@ def test_mask_counts_at_8k_match_hand_derived():
         p = config2(kind, Hq=1, Hkv=1)
         got = int(oracle.mask_row_counts(p).sum())
         assert got == n, (kind, got, n)
+
+
+# ------------------------------------------------------------ row-local helpers
+@pytest.mark.parametrize("prob", ALL_TINY + [cases.shard_problem([7, 12], [[3, 4], [5, 7]])[0]],
+                         ids=[p.name for p in ALL_TINY] + ["shards"])
+def test_row_local_helpers_match_full_backward(prob):
+    """forward_rows / backward_rows / key_grads_from_rows, summed over all rows
+    and heads, reproduce the full forward and backward."""
+    q, k, v, do = _rand(prob, 17)
+    O, L = oracle.attention_forward(prob, q, k, v)
+    dQ, dK, dV = oracle.attention_backward(prob, q, k, v, do)
+    G = prob.Hq // prob.Hkv
+    dK2, dV2 = np.zeros_like(dK), np.zeros_like(dV)
+    for s, seg in enumerate(prob.segments):
+        rows = np.arange(seg.q_len)
+        if seg.q_len == 0:
+            continue
+        for h in range(prob.Hq):
+            o, lse = oracle.forward_rows(prob, q, k, v, s, h, rows)
+            np.testing.assert_allclose(o, O[seg.q_off:seg.q_off + seg.q_len, h], atol=1e-12)
+            np.testing.assert_allclose(lse, L[h, seg.q_off:seg.q_off + seg.q_len], atol=1e-12)
+            dq = oracle.backward_rows(prob, q, k, v, do, s, h, rows)
+            np.testing.assert_allclose(dq, dQ[seg.q_off:seg.q_off + seg.q_len, h], atol=1e-12)
+            cols = np.arange(seg.k_len)
+            # split the rows in two halves to exercise partial sums
+            for part in (rows[: len(rows) // 2], rows[len(rows) // 2:]):
+                if len(part) == 0:
+                    continue
+                a, b = oracle.key_grads_from_rows(prob, q, k, v, do, s, h, part, cols)
+                dK2[seg.k_off:seg.k_off + seg.k_len, h // G] += a
+                dV2[seg.k_off:seg.k_off + seg.k_len, h // G] += b
+    np.testing.assert_allclose(dK2, dK, atol=1e-12)
+    np.testing.assert_allclose(dV2, dV, atol=1e-12)
