@@ -14,17 +14,21 @@
 // GB300 mapping.  One persistent CTA per SM, 10 warps:
 //   warp 9       TMA producer: claims work items from the cost-sorted list
 //                through an atomic counter, loads Q (two 128-row sub-tiles)
-//                and streams K/V tiles through a 3-stage ring;
-//   warp 8       MMA issuer: S_x = Q_x K^T and O_x += P_x V with tcgen05.mma,
-//                accumulators in TMEM (S0, S1, O0, O1: 4 x 128 columns);
+//                and streams K, V tiles through a 5-stage ring;
+//   warp 8       MMA issuer: S_x = Q_x K^T and O_x += P_x V with tcgen05.mma;
+//                TMEM holds S0, S1, O0, O1 (4 x 128 columns) and P_x (bf16)
+//                overwrites the first 64 columns of S_x once the softmax has
+//                read it, so O_x += P_x V reads its A operand from TMEM;
 //   warps 0-7    two softmax warpgroups, one per 128-row sub-tile; thread r
 //                owns TMEM lane r (row r): it reads the score row, applies
 //                the mask, runs the online softmax in base 2, rescales O in
 //                TMEM only when its running max grows by more than 2^8,
-//                writes P (bf16) to shared memory, and at the end normalises
-//                O and writes O and LSE.
-// While one warpgroup computes exponentials the tensor core runs the other
-// sub-tile's products.
+//                writes P back into TMEM, and at the end normalises O and
+//                writes O and LSE.
+// Per sub-tile the MMA thread issues O_x += P_x(t-1) V(t-1) and then
+// S_x(t) = Q_x K(t)^T (tcgen05.mma executes in issue order, so S_x(t) does not
+// overwrite P_x(t-1) before it is read); while one warpgroup computes
+// exponentials the tensor core runs the other sub-tile's products.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -35,13 +39,12 @@ namespace lca {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr uint32_t kTileBytes = 32768;   // 128 rows x 128 bf16
 constexpr uint32_t kChunkBytes = 16384;  // 128 rows x 64 bf16: one 128-byte-swizzled TMA box
 constexpr int kOffQ = 0;                 // Q sub-tile x at x * kTileBytes
 constexpr int kOffKV = 2 * kTileBytes;   // K/V ring
-constexpr int kOffP = kOffKV + kStages * kTileBytes;  // P sub-tile x at + x * kTileBytes
-constexpr int kOffCtl = kOffP + 2 * kTileBytes;
+constexpr int kOffCtl = kOffKV + kStages * kTileBytes;
 constexpr int kSmemBytes = kOffCtl + 1024 + 1024;  // control block + alignment slack
 
 enum : int {
@@ -50,8 +53,7 @@ enum : int {
   B_KVFULL = 2,
   B_KVEMPTY = B_KVFULL + kStages,
   B_SFULL = B_KVEMPTY + kStages,
-  B_SEMPTY = B_SFULL + 2,
-  B_PFULL = B_SEMPTY + 2,
+  B_PFULL = B_SFULL + 2,
   B_OFULL = B_PFULL + 2,
   B_ITFULL = B_OFULL + 2,
   B_ITEMPTY = B_ITFULL + 2,
@@ -65,16 +67,13 @@ struct Item {  // 32 bytes, broadcast from the producer to the other roles
 };
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T (both K-major)
-constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);   // O += P V (V is N-major)
+constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);   // O += P V (P in TMEM, V N-major)
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// Ring position of the u-th load of an item with n tiles: loads follow the
-// order the MMA warp consumes them: K0, K1, V0, K2, V1, ..., K(n-1), V(n-2), V(n-1).
-__device__ __forceinline__ uint32_t k_load_index(int t) { return t == 0 ? 0u : static_cast<uint32_t>(2 * t - 1); }
-__device__ __forceinline__ uint32_t v_load_index(int t, int n) {
-  return (t == n - 1) ? static_cast<uint32_t>(2 * n - 1) : static_cast<uint32_t>(2 * t + 2);
-}
+// Loads and the MMA warp's uses follow the same order: K0, V0, K1, V1, ...
+__device__ __forceinline__ uint32_t k_load_index(int t) { return static_cast<uint32_t>(2 * t); }
+__device__ __forceinline__ uint32_t v_load_index(int t) { return static_cast<uint32_t>(2 * t + 1); }
 
 __device__ __forceinline__ bool wait1(uint64_t* bar, uint32_t parity, const AttnArgs& a, int where) {
   return mbar_wait(bar, parity, a.status, a.wait_limit_ns, kStatusTimeout, where);
@@ -132,25 +131,22 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
 
       const int g = inf.head / pv.G;
       const int n = inf.cnt;
-      for (int u = 0; u < 2 * n; ++u) {
-        int t;
-        bool is_v;
-        if (u == 0) { t = 0; is_v = false; }
-        else if (u & 1) {
-          t = (u + 1) >> 1;
-          is_v = (t >= n);
-          if (is_v) t = n - 1;
-        } else { t = (u >> 1) - 1; is_v = true; }
-        const int kt = static_cast<int>(entries[inf.ebase + t] & 0xFFFFFFu);
-        const uint32_t idx = kv_iter + u;
-        const int stg = idx % kStages;
-        if (idx >= kStages && !wait1(&bar[B_KVEMPTY + stg], ((idx / kStages) - 1) & 1, a, 12)) goto abort;
-        mbar_arrive_expect_tx(&bar[B_KVFULL + stg], kTileBytes);
-        const CUtensorMap* m = is_v ? tv : tk;
-        const int yk = sg.k_off + kt * kTile;
-        tma_load_2d(sKV + stg * kTileBytes, m, &bar[B_KVFULL + stg], g * kHeadDim, yk);
-        tma_load_2d(sKV + stg * kTileBytes + kChunkBytes, m, &bar[B_KVFULL + stg], g * kHeadDim + 64, yk);
-        issued = idx + 1;
+      uint32_t e_next = (n > 0) ? entries[inf.ebase] : 0u;
+      for (int t = 0; t < n; ++t) {
+        const uint32_t e = e_next;
+        if (t + 1 < n) e_next = entries[inf.ebase + t + 1];
+        const int yk = sg.k_off + static_cast<int>(e & 0xFFFFFFu) * kTile;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {  // K(t) then V(t)
+          const uint32_t idx = kv_iter + 2 * t + which;
+          const int stg = idx % kStages;
+          if (idx >= kStages && !wait1(&bar[B_KVEMPTY + stg], ((idx / kStages) - 1) & 1, a, 12)) goto abort;
+          mbar_arrive_expect_tx(&bar[B_KVFULL + stg], kTileBytes);
+          const CUtensorMap* m = which ? tv : tk;
+          tma_load_2d(sKV + stg * kTileBytes, m, &bar[B_KVFULL + stg], g * kHeadDim, yk);
+          tma_load_2d(sKV + stg * kTileBytes + kChunkBytes, m, &bar[B_KVFULL + stg], g * kHeadDim + 64, yk);
+          issued = idx + 1;
+        }
       }
       kv_iter += 2 * n;
     }
@@ -165,16 +161,15 @@ abort:
 }
 
 // ------------------------------------------------------------------ MMA issuer
-__device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8_t* sKV, uint8_t* sP, uint64_t* bar,
-                                           Item* items, uint32_t tbase) {
+__device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8_t* sKV, uint64_t* bar, Item* items,
+                                           uint32_t tbase) {
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
   // operand descriptors built once; every MMA below only adds a byte offset
   const uint64_t dQ0 = sdesc_sw128(smem_u32(sQ), 16, 1024);           // Q_x, K-major
   const uint64_t dK0 = sdesc_sw128(smem_u32(sKV), 16, 1024);          // K tile, K-major
   const uint64_t dV0 = sdesc_sw128(smem_u32(sKV), kChunkBytes, 1024); // V tile, N-major
-  const uint64_t dP0 = sdesc_sw128(smem_u32(sP), 16, 1024);           // P_x, K-major
   uint32_t kv_iter = 0;
-  uint32_t s_iss[2] = {0, 0}, p_iss[2] = {0, 0};
+  uint32_t p_iss[2] = {0, 0};
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 20)) goto abort;
@@ -189,57 +184,48 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
       uint32_t e_cur = (n > 0) ? entries[inf.ebase] : 0u, e_prev = 0u;
       for (int t = 0; t <= n; ++t) {
         const uint32_t e_nxt = (t + 1 < n) ? entries[inf.ebase + t + 1] : 0u;
-        if (t < n) {  // S_x(t) = Q_x K(t)^T
-          const uint32_t e = e_cur;
-          const uint32_t idx = kv_iter + k_load_index(t);
-          const int stg = idx % kStages;
-          if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 22)) goto abort;
-          tc_fence_after();
-          const uint64_t dK = desc_add(dK0, stg * kTileBytes);
+        const uint32_t vidx = kv_iter + v_load_index(t - 1), kidx = kv_iter + k_load_index(t);
+        const int vst = vidx % kStages, kst = kidx % kStages;
+        bool v_ready = false, k_ready = false;
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (((e >> (24 + 2 * x)) & 3u) == 0) continue;
-            if (s_iss[x] >= 1 && !wait1(&bar[B_SEMPTY + x], (s_iss[x] - 1) & 1, a, 23)) goto abort;
+        for (int x = 0; x < 2; ++x) {
+          const uint32_t tS = tbase + 128 * x, tO = tbase + 256 + 128 * x;
+          if (t >= 1 && ((e_prev >> (24 + 2 * x)) & 3u) != 0) {  // O_x += P_x(t-1) V(t-1), P_x from TMEM
+            if (!v_ready) {
+              if (!wait1(&bar[B_KVFULL + vst], (vidx / kStages) & 1, a, 24)) goto abort;
+              v_ready = true;
+            }
+            if (!wait1(&bar[B_PFULL + x], p_iss[x] & 1, a, 25)) goto abort;
             tc_fence_after();
+            const uint64_t dV = desc_add(dV0, vst * kTileBytes);
+            const uint32_t acc0 = first_pv[x] ? 0u : 1u;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_ts(tO, tS + 8 * ks, desc_add(dV, ks * 2048), kIdescO, ks > 0 ? 1u : acc0);
+            first_pv[x] = false;
+            umma_commit(&bar[B_OFULL + x]);
+            ++p_iss[x];
+          }
+          if (t < n && ((e_cur >> (24 + 2 * x)) & 3u) != 0) {  // S_x(t) = Q_x K(t)^T, after PV_x(t-1)
+            if (!k_ready) {
+              if (!wait1(&bar[B_KVFULL + kst], (kidx / kStages) & 1, a, 22)) goto abort;
+              k_ready = true;
+            }
+            tc_fence_after();
+            const uint64_t dK = desc_add(dK0, kst * kTileBytes);
             const uint64_t dQx = desc_add(dQ0, x * kTileBytes);
-            const uint32_t tS = tbase + 128 * x;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
               const uint32_t koff = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
               umma_ss(tS, desc_add(dQx, koff), desc_add(dK, koff), kIdescS, ks > 0 ? 1u : 0u);
             }
             umma_commit(&bar[B_SFULL + x]);
-            ++s_iss[x];
           }
-          umma_commit(&bar[B_KVEMPTY + stg]);
-          if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
         }
-        if (t >= 1) {  // O_x += P_x(t-1) V(t-1)
-          const int u = t - 1;
-          const uint32_t e = e_prev;
-          const uint32_t idx = kv_iter + v_load_index(u, n);
-          const int stg = idx % kStages;
-          if (!wait1(&bar[B_KVFULL + stg], (idx / kStages) & 1, a, 24)) goto abort;
-          tc_fence_after();
-          const uint64_t dV = desc_add(dV0, stg * kTileBytes);
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (((e >> (24 + 2 * x)) & 3u) == 0) continue;
-            if (!wait1(&bar[B_PFULL + x], p_iss[x] & 1, a, 25)) goto abort;
-            tc_fence_after();
-            const uint64_t dPx = desc_add(dP0, x * kTileBytes);
-            const uint32_t tO = tbase + 256 + 128 * x;
-            const uint32_t acc0 = first_pv[x] ? 0u : 1u;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-              const uint32_t poff = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
-              umma_ss(tO, desc_add(dPx, poff), desc_add(dV, ks * 2048), kIdescO, ks > 0 ? 1u : acc0);
-            }
-            first_pv[x] = false;
-            umma_commit(&bar[B_OFULL + x]);
-            ++p_iss[x];
-          }
-          umma_commit(&bar[B_KVEMPTY + stg]);
+        if (t >= 1) umma_commit(&bar[B_KVEMPTY + vst]);
+        if (t < n) {
+          umma_commit(&bar[B_KVEMPTY + kst]);
+          if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
         }
         e_prev = e_cur;
         e_cur = e_nxt;
@@ -254,8 +240,7 @@ abort:
 }
 
 // ------------------------------------------------------------------ softmax warpgroup
-__device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP, uint64_t* bar, Item* items,
-                                           uint32_t tbase) {
+__device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
   const int wq = (threadIdx.x >> 5) & 3;
@@ -264,7 +249,6 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
   const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
   const uint32_t tS = tbase + tl + 128 * x;
   const uint32_t tO = tbase + tl + 256 + 128 * x;
-  uint8_t* myP = sP + x * kTileBytes;
   __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o);
   const float sl2 = a.scale_log2;
   uint32_t s_cons = 0, p_prod = 0;
@@ -288,6 +272,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
       if (cls == kTileEmpty) continue;
       const int kt = static_cast<int>(e & 0xFFFFFFu);
       if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
+      ++s_cons;
       tc_fence_after();
       float s[128];
 #pragma unroll
@@ -298,10 +283,6 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
         for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(r[k]);
       }
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_SEMPTY + x]);
-      ++s_cons;
       if (cls == kTilePartial) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -323,25 +304,27 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
         need = true;
         m_use = m_new;
       }
-      // P = exp2(s*scale*log2e - m) in bf16; computed before waiting for the
-      // previous PV so that the score registers are free during the wait
+      // P = exp2(s*scale*log2e - m) as bf16 pairs, written over the first 64
+      // columns of S_x in TMEM (the A operand of O_x += P_x V)
       const float base = (m_use == -INFINITY) ? 0.f : m_use;
       float sum = 0.f;
-      uint32_t pk[64];
 #pragma unroll
-      for (int k = 0; k < 64; ++k) {
-        const float p0 = ex2_approx(fmaf(s[2 * k], sl2, -base));
-        const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, -base));
-        sum += p0 + p1;
-        pk[k] = pack_bf16x2(p0, p1);
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = ex2_approx(fmaf(s[64 * h + 2 * k], sl2, -base));
+          const float p1 = ex2_approx(fmaf(s[64 * h + 2 * k + 1], sl2, -base));
+          sum += p0 + p1;
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + 32 * h, pk);
       }
       l = l * factor + sum;
-      if (any) {
-        // the previous O_x += P_x V has finished: P_x may be overwritten and O_x is stable
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        // the previous O_x += P_x V must have finished before O_x is rescaled
         if (!waitw(&bar[B_OFULL + x], (p_prod - 1) & 1, a, 34 + x)) return;
         tc_fence_after();
-      }
-      if (__any_sync(0xFFFFFFFFu, need)) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -351,18 +334,8 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint8_t* sP
           for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * factor);
           tmem_st32(tO + 32 * c, r);
         }
-        tmem_st_wait();
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle the MMA expects
-#pragma unroll
-      for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = make_uint4(pk[32 * kc + 4 * u], pk[32 * kc + 4 * u + 1], pk[32 * kc + 4 * u + 2],
-                                     pk[32 * kc + 4 * u + 3]);
-          *reinterpret_cast<uint4*>(myP + kc * kChunkBytes + row * 128 + ((u ^ (row & 7)) << 4)) = v;
-        }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_PFULL + x]);
@@ -411,7 +384,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + kOffQ;
   uint8_t* sKV = sm + kOffKV;
-  uint8_t* sP = sm + kOffP;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
   Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
@@ -423,21 +395,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (threadIdx.x == 0) {
-    mbar_init(&bar[B_QFULL], 1);
-    mbar_init(&bar[B_QEMPTY], 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar[B_KVFULL + s], 1);
-      mbar_init(&bar[B_KVEMPTY + s], 1);
-    }
+    for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&bar[B_SFULL + x], 1);
-      mbar_init(&bar[B_SEMPTY + x], 4);  // one arrival per softmax warp
-      mbar_init(&bar[B_PFULL + x], 4);
-      mbar_init(&bar[B_OFULL + x], 1);
-      mbar_init(&bar[B_ITFULL + x], 1);
+      mbar_init(&bar[B_PFULL + x], 4);  // one arrival per softmax warp
       mbar_init(&bar[B_ITEMPTY + x], 9);
     }
-    mbar_init(&bar[B_DRAIN], 1);
     fence_mbar_init();
   }
   if (warp == 9 && lane == 0) {
@@ -453,9 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     if (lane == 0) producer(a, &tmQ, &tmK, &tmV, sQ, sKV, bar, items);
   } else if (warp == 8) {
-    if (lane == 0) mma_issuer(a, sQ, sKV, sP, bar, items, tbase);
+    if (lane == 0) mma_issuer(a, sQ, sKV, bar, items, tbase);
   } else {
-    softmax_wg(a, warp >> 2, sP, bar, items, tbase);
+    softmax_wg(a, warp >> 2, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
