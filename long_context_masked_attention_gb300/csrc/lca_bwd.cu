@@ -371,14 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ====================================================================== dK / dV
 namespace dkv {
 
-constexpr int kRing = 3;                        // Q/dO (and staged statistics) ring depth
+constexpr int kRing = 4;                        // Q/dO (and staged statistics) ring depth
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTile128;
 constexpr int kOffQ = kOffV + kTile128;          // ring of 64-row Q tiles
 constexpr int kOffDO = kOffQ + kRing * kTile64;  // ring of 64-row dO tiles
-constexpr int kOffP = kOffDO + kRing * kTile64;  // P^T  [128 keys x 64 queries]
-constexpr int kOffDS = kOffP + kTile64;          // dS^T
-constexpr int kOffStat = kOffDS + kTile64;       // kRing buffers of: lse2[64], D[64], mask words[64][4], meta
+constexpr int kOffStat = kOffDO + kRing * kTile64;  // kRing buffers of: lse2[64], D[64], mask words[64][4], meta
 constexpr int kStatBytes = 64 * 4 * 2 + 64 * 4 * 4 + 16;
 constexpr int kOffCtl = kOffStat + kRing * kStatBytes;
 constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
@@ -386,7 +384,7 @@ constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
 enum : int {
   B_KVFULL = 0, B_KVEMPTY,
   B_QFULL, B_QEMPTY = B_QFULL + kRing, B_MFULL = B_QEMPTY + kRing, B_MEMPTY = B_MFULL + kRing,
-  B_SFULL = B_MEMPTY + kRing, B_SEMPTY = B_SFULL + 2, B_PFULL = B_SEMPTY + 2, B_PEMPTY, B_ACCFULL,
+  B_SFULL = B_MEMPTY + kRing, B_PFULL = B_SFULL + 2, B_ACCFULL = B_PFULL + 2,
   B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_DRAIN = B_ITEMPTY + 2, B_COUNT
 };
 
@@ -570,8 +568,6 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
   const uint64_t dOk = sdesc_sw128(base + kOffDO, 16, 1024);        // dO ring, K-major (B of dP^T)
   const uint64_t dQn = sdesc_sw128(base + kOffQ, kChunk64, 1024);   // Q ring, N-major (B of dK)
   const uint64_t dOn = sdesc_sw128(base + kOffDO, kChunk64, 1024);  // dO ring, N-major (B of dV)
-  const uint64_t dPk = sdesc_sw128(base + kOffP, 16, 1024);
-  const uint64_t dSk = sdesc_sw128(base + kOffDS, 16, 1024);
   uint32_t steps = 0;  // global step counter (rings and TMEM double buffers)
   int acc_items = 0;
   for (int it = 0;; ++it) {
@@ -586,9 +582,10 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
       const int n = inf.nsteps;
       for (int p = 0; p <= n; ++p) {
         if (p < n) {  // S^T = K Q^T, dP^T = V dO^T into TMEM buffer b, from ring slot r
+          // Buffer b last held P^T / dS^T of step idx-2, whose dV/dK products were
+          // issued earlier from this thread; MMAs run in issue order, so no wait.
           const uint32_t idx = steps + p;
           const int b = idx & 1, r = idx % kRing;
-          if (idx >= 2 && !wait1(&bar[B_SEMPTY + b], ((idx >> 1) - 1) & 1, a, 222)) goto abort;
           if (!wait1(&bar[B_QFULL + r], (idx / kRing) & 1, a, 223)) goto abort;
           tc_fence_after();
           const uint64_t dQ = desc_add(dQk, r * kTile64), dO = desc_add(dOk, r * kTile64);
@@ -608,20 +605,22 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           umma_commit(&bar[B_SFULL + b]);
           if (p == n - 1) umma_commit(&bar[B_KVEMPTY]);
         }
-        if (p >= 1) {  // dV += P^T dO, dK += dS^T Q for step p-1
+        if (p >= 1) {  // dV += P^T dO, dK += dS^T Q for step p-1, P^T and dS^T read from TMEM
           const uint32_t idx = steps + p - 1;
-          const int r = idx % kRing;
-          if (!wait1(&bar[B_PFULL], idx & 1, a, 224)) goto abort;
+          const int b = idx & 1, r = idx % kRing;
+          if (!wait1(&bar[B_PFULL + b], (idx >> 1) & 1, a, 224)) goto abort;
           tc_fence_after();
           const uint64_t dQ = desc_add(dQn, r * kTile64), dO = desc_add(dOn, r * kTile64);
           const uint32_t acc = (p > 1) ? 1u : 0u;
+          // queries 16ks..16ks+15 sit in columns 32*(ks/2) + 8*(ks%2) of the buffer (bf16 pairs)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_ss(tbase + 256, desc_add(dPk, ks * 32), desc_add(dO, ks * 2048), kIdescMN, (ks > 0) ? 1u : acc);
+            umma_ts(tbase + 256, tbase + 64 * b + 32 * (ks >> 1) + 8 * (ks & 1), desc_add(dO, ks * 2048), kIdescMN,
+                    (ks > 0) ? 1u : acc);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_ss(tbase + 384, desc_add(dSk, ks * 32), desc_add(dQ, ks * 2048), kIdescMN, (ks > 0) ? 1u : acc);
-          umma_commit(&bar[B_PEMPTY]);
+            umma_ts(tbase + 384, tbase + 128 + 64 * b + 32 * (ks >> 1) + 8 * (ks & 1), desc_add(dQ, ks * 2048),
+                    kIdescMN, (ks > 0) ? 1u : acc);
           umma_commit(&bar[B_QEMPTY + r]);
           if (p == n) umma_commit(&bar[B_ACCFULL]);
         }
@@ -675,9 +674,6 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
       }
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_SEMPTY + b]);
       if (cls == kTilePartial) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
@@ -696,22 +692,14 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_MEMPTY + r]);  // done with this step's staged data
-      // the previous step's dV/dK products have read P^T and dS^T
-      if (steps >= 1 && !waitw(&bar[B_PEMPTY], (steps - 1) & 1, a, 232)) return;
-      // P^T and dS^T rows: [128 keys x 64 queries], K-major, one 128-byte swizzle chunk;
-      // this thread writes the 4 x 16-byte pieces of its 32 query columns.
-      uint8_t* pbuf = sm + kOffP;
-      uint8_t* dbuf = sm + kOffDS;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int piece = 4 * half + u;
-        const uint32_t off = j * 128 + ((piece ^ (j & 7)) << 4);
-        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pp[4 * u], pp[4 * u + 1], pp[4 * u + 2], pp[4 * u + 3]);
-        *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
-      }
-      fence_proxy_async_smem();
+      // P^T and dS^T (bf16 pairs) go over the first 16 of the 32 S^T / dP^T
+      // columns this thread just read; the dV/dK products take them from there.
+      tmem_st16(tbase + tl + 64 * b + 32 * half, pp);
+      tmem_st16(tbase + tl + 128 + 64 * b + 32 * half, pd);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_PFULL]);
+      if (lane == 0) mbar_arrive(&bar[B_PFULL + b]);
     }
     // epilogue: rows of the key group only
     const int jg = inf.kt * kTile + j;
@@ -769,8 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (threadIdx.x == 0) {
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
-    for (int b = 0; b < 2; ++b) mbar_init(&bar[B_SEMPTY + b], 8);  // one arrival per compute warp
-    mbar_init(&bar[B_PFULL], 8);
+    for (int b = 0; b < 2; ++b) mbar_init(&bar[B_PFULL + b], 8);  // one arrival per compute warp
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&bar[B_MEMPTY + r], 8);
       mbar_init(&bar[B_MFULL + r], 33);  // 32 cp.async completions + the producer's own arrive
