@@ -165,20 +165,20 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
   uint32_t sdp = 0;    // S/dP products issued (TMEM reuse count)
   for (int it = 0;; ++it) {
     const int slot = it & 1;
-    if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 120)) goto abort;
+    if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 120)) goto abort;
     {
       const Item inf = items[slot];
-      mbar_arrive(&bar[B_ITEMPTY + slot]);
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
       if (!inf.valid) return;
-      if (!wait1(&bar[B_QFULL], it & 1, a, 121)) goto abort;
+      if (!waitw(&bar[B_QFULL], it & 1, a, 121)) goto abort;
       tc_fence_after();
       const int n = inf.cnt;
       for (int t = 0; t <= n; ++t) {
         if (t < n) {  // S = Q K^T, dP = dO V^T for key tile t
           const uint32_t idx = tiles + t;
           const int kr = idx % kKRing, vr = idx % kVRing;
-          if (sdp >= 1 && !wait1(&bar[B_SEMPTY], (sdp - 1) & 1, a, 122)) goto abort;
-          if (!wait1(&bar[B_KFULL + kr], (idx / kKRing) & 1, a, 123)) goto abort;
+          if (sdp >= 1 && !waitw(&bar[B_SEMPTY], (sdp - 1) & 1, a, 122)) goto abort;
+          if (!waitw(&bar[B_KFULL + kr], (idx / kKRing) & 1, a, 123)) goto abort;
           tc_fence_after();
           const uint64_t dK = desc_add(dKk, kr * kTile128);
 #pragma unroll
@@ -186,7 +186,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
             const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
             umma_ss(tbase + 0, desc_add(dQd, off), desc_add(dK, off), kIdesc128, ks > 0);
           }
-          if (!wait1(&bar[B_VFULL + vr], (idx / kVRing) & 1, a, 124)) goto abort;
+          if (!waitw(&bar[B_VFULL + vr], (idx / kVRing) & 1, a, 124)) goto abort;
           tc_fence_after();
           const uint64_t dV = desc_add(dVk, vr * kTile128);
 #pragma unroll
@@ -202,7 +202,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
         if (t >= 1) {  // dQ += dS K for key tile t-1, dS read from TMEM
           const uint32_t idx = tiles + t - 1;
           const int db = idx & 1, kr = idx % kKRing;
-          if (!wait1(&bar[B_DSFULL + db], (idx >> 1) & 1, a, 125)) goto abort;
+          if (!waitw(&bar[B_DSFULL + db], (idx >> 1) & 1, a, 125)) goto abort;
           tc_fence_after();
           const uint64_t dK = desc_add(dKn, kr * kTile128);
           const uint32_t tA = tbase + 384 + 64 * db;
@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     if (lane == 0) producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
   } else if (warp == 8) {
-    if (lane == 0) mma_issuer(a, sm, bar, items, tbase);
+    mma_issuer(a, sm, bar, items, tbase);
   } else {
     compute(a, sm, bar, items, tbase);
   }
@@ -572,12 +572,12 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
   int acc_items = 0;
   for (int it = 0;; ++it) {
     const int slot = it & 1;
-    if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 220)) goto abort;
+    if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 220)) goto abort;
     {
       const Item inf = items[slot];
-      mbar_arrive(&bar[B_ITEMPTY + slot]);
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
       if (!inf.valid) return;
-      if (!wait1(&bar[B_KVFULL], it & 1, a, 221)) goto abort;
+      if (!waitw(&bar[B_KVFULL], it & 1, a, 221)) goto abort;
       tc_fence_after();
       const int n = inf.nsteps;
       for (int p = 0; p <= n; ++p) {
@@ -586,7 +586,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           // issued earlier from this thread; MMAs run in issue order, so no wait.
           const uint32_t idx = steps + p;
           const int b = idx & 1, r = idx % kRing;
-          if (!wait1(&bar[B_QFULL + r], (idx / kRing) & 1, a, 223)) goto abort;
+          if (!waitw(&bar[B_QFULL + r], (idx / kRing) & 1, a, 223)) goto abort;
           tc_fence_after();
           const uint64_t dQ = desc_add(dQk, r * kTile64), dO = desc_add(dOk, r * kTile64);
           const uint32_t tS = tbase + 64 * b, tP = tbase + 128 + 64 * b;
@@ -608,7 +608,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
         if (p >= 1) {  // dV += P^T dO, dK += dS^T Q for step p-1, P^T and dS^T read from TMEM
           const uint32_t idx = steps + p - 1;
           const int b = idx & 1, r = idx % kRing;
-          if (!wait1(&bar[B_PFULL + b], (idx >> 1) & 1, a, 224)) goto abort;
+          if (!waitw(&bar[B_PFULL + b], (idx >> 1) & 1, a, 224)) goto abort;
           tc_fence_after();
           const uint64_t dQ = desc_add(dQn, r * kTile64), dO = desc_add(dOn, r * kTile64);
           const uint32_t acc = (p > 1) ? 1u : 0u;
@@ -773,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
   } else if (warp == 8) {
-    if (lane == 0) mma_issuer(a, sm, bar, items, tbase);
+    mma_issuer(a, sm, bar, items, tbase);
   } else {
     compute(a, sm, bar, items, tbase);
   }

@@ -172,12 +172,12 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
   uint32_t p_iss[2] = {0, 0};
   for (int it = 0;; ++it) {
     const int slot = it & 1;
-    if (!wait1(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 20)) goto abort;
+    if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 20)) goto abort;
     {
       const Item inf = items[slot];
-      mbar_arrive(&bar[B_ITEMPTY + slot]);
+      if ((threadIdx.x & 31) == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
       if (!inf.valid) return;
-      if (!wait1(&bar[B_QFULL], it & 1, a, 21)) goto abort;
+      if (!waitw(&bar[B_QFULL], it & 1, a, 21)) goto abort;
       tc_fence_after();
       const int n = inf.cnt;
       bool first_pv[2] = {true, true};
@@ -192,10 +192,10 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
           const uint32_t tS = tbase + 128 * x, tO = tbase + 256 + 128 * x;
           if (t >= 1 && ((e_prev >> (24 + 2 * x)) & 3u) != 0) {  // O_x += P_x(t-1) V(t-1), P_x from TMEM
             if (!v_ready) {
-              if (!wait1(&bar[B_KVFULL + vst], (vidx / kStages) & 1, a, 24)) goto abort;
+              if (!waitw(&bar[B_KVFULL + vst], (vidx / kStages) & 1, a, 24)) goto abort;
               v_ready = true;
             }
-            if (!wait1(&bar[B_PFULL + x], p_iss[x] & 1, a, 25)) goto abort;
+            if (!waitw(&bar[B_PFULL + x], p_iss[x] & 1, a, 25)) goto abort;
             tc_fence_after();
             const uint64_t dV = desc_add(dV0, vst * kTileBytes);
             const uint32_t acc0 = first_pv[x] ? 0u : 1u;
@@ -208,7 +208,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
           }
           if (t < n && ((e_cur >> (24 + 2 * x)) & 3u) != 0) {  // S_x(t) = Q_x K(t)^T, after PV_x(t-1)
             if (!k_ready) {
-              if (!wait1(&bar[B_KVFULL + kst], (kidx / kStages) & 1, a, 22)) goto abort;
+              if (!waitw(&bar[B_KVFULL + kst], (kidx / kStages) & 1, a, 22)) goto abort;
               k_ready = true;
             }
             tc_fence_after();
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 9) {
     if (lane == 0) producer(a, &tmQ, &tmK, &tmV, sQ, sKV, bar, items);
   } else if (warp == 8) {
-    if (lane == 0) mma_issuer(a, sQ, sKV, bar, items, tbase);
+    mma_issuer(a, sQ, sKV, bar, items, tbase);
   } else {
     softmax_wg(a, warp >> 2, bar, items, tbase);
   }
