@@ -240,6 +240,74 @@ abort:
 }
 
 // ------------------------------------------------------------------ softmax warpgroup
+// The softmax reads a 128-column S row from TMEM twice (once for the row
+// maximum, once for the exponentials) in 32-column chunks, so that only two
+// chunks are live in registers at a time.
+//
+// Score of column k of a chunk, -inf where the mask word clears it.
+template <bool kMasked>
+__device__ __forceinline__ float score(uint32_t raw, uint32_t bits, int k) {
+  return (!kMasked || ((bits >> k) & 1u)) ? __uint_as_float(raw) : -INFINITY;
+}
+
+// Row maximum of the 128 scores: eight independent partial maxima (3-input
+// max) so the reduction is not one 128-long dependency chain.
+template <bool kMasked>
+__device__ __forceinline__ float tile_row_max(uint32_t tS, const uint32_t (&mb)[4]) {
+  float mp[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+#pragma unroll
+  for (int cp = 0; cp < 2; ++cp) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tS + 64 * cp, r0);
+    tmem_ld32(tS + 64 * cp + 32, r1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        mp[j] = fmax3(mp[j], score<kMasked>(r0[16 * g + j], mb[2 * cp], 16 * g + j),
+                      score<kMasked>(r0[16 * g + 8 + j], mb[2 * cp], 16 * g + 8 + j));
+        mp[j] = fmax3(mp[j], score<kMasked>(r1[16 * g + j], mb[2 * cp + 1], 16 * g + j),
+                      score<kMasked>(r1[16 * g + 8 + j], mb[2 * cp + 1], 16 * g + 8 + j));
+      }
+    }
+  }
+  return fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+}
+
+// P = 2^(s*scale*log2(e) - base) for the thread's row, written as bf16 pairs
+// over the first 64 columns of S in TMEM (chunk c's 16 pair-columns land on
+// columns 16c..16c+15, which belong to chunks already read); returns the row
+// sum of P in f32.
+template <bool kMasked>
+__device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], float sl2, float base) {
+  const uint64_t sl2x2 = f2(sl2, sl2), nb2 = f2(-base, -base);
+  uint64_t acc[4] = {0, 0, 0, 0};  // four independent packed partial sums
+  uint32_t ra[32], rb[32];
+  tmem_ld32(tS, ra);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    tmem_ld_wait();
+    uint32_t(&cur)[32] = (c & 1) ? rb : ra;
+    uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
+    if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), nxt);
+    uint32_t pk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const uint64_t sv = f2(score<kMasked>(cur[2 * k], mb[c], 2 * k), score<kMasked>(cur[2 * k + 1], mb[c], 2 * k + 1));
+      const uint64_t xx = ffma2(sv, sl2x2, nb2);
+      const uint64_t pp = f2(ex2_approx(f2lo(xx)), ex2_approx(f2hi(xx)));
+      acc[k & 3] = fadd2(acc[k & 3], pp);
+      pk[k] = pack_bf16x2(f2lo(pp), f2hi(pp));
+    }
+    tmem_st16(tS + 16 * c, pk);
+  }
+  const uint64_t t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return f2lo(t) + f2hi(t);
+}
+
 __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
@@ -271,29 +339,16 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       const uint32_t cls = (e >> (24 + 2 * x)) & 3u;
       if (cls == kTileEmpty) continue;
       const int kt = static_cast<int>(e & 0xFFFFFFu);
+      // mask words of a partial tile, computed while S is still being produced
+      uint32_t mb[4] = {~0u, ~0u, ~0u, ~0u};
+      if (cls == kTilePartial) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) mb[c] = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
+      }
       if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
       ++s_cons;
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + 32 * c, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[32 * c + k] = __uint_as_float(r[k]);
-      }
-      tmem_ld_wait();
-      if (cls == kTilePartial) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t bits = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
-#pragma unroll
-          for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
-        }
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int k = 0; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      const float mx = (cls == kTilePartial) ? tile_row_max<true>(tS, mb) : tile_row_max<false>(tS, mb);
       const float m_new = fmaxf(m_use, mx * sl2);
       float factor = 1.f;
       bool need = false;
@@ -307,19 +362,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       // P = exp2(s*scale*log2e - m) as bf16 pairs, written over the first 64
       // columns of S_x in TMEM (the A operand of O_x += P_x V)
       const float base = (m_use == -INFINITY) ? 0.f : m_use;
-      float sum = 0.f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = ex2_approx(fmaf(s[64 * h + 2 * k], sl2, -base));
-          const float p1 = ex2_approx(fmaf(s[64 * h + 2 * k + 1], sl2, -base));
-          sum += p0 + p1;
-          pk[k] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(tS + 32 * h, pk);
-      }
+      const float sum = (cls == kTilePartial) ? tile_exp<true>(tS, mb, sl2, base) : tile_exp<false>(tS, mb, sl2, base);
       l = l * factor + sum;
       if (__any_sync(0xFFFFFFFFu, need)) {
         // the previous O_x += P_x V must have finished before O_x is rescaled
