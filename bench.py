@@ -263,7 +263,7 @@ def run_ours(args):
 
     # ---- timed region: device-resident inputs, L2 flushed between steps
     n_calls = 2 * len(probs) * args.steps
-    kev = lca.KernelEvents(4 * n_calls + 8)
+    kev = lca.KernelEvents(5 * n_calls + 8)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])

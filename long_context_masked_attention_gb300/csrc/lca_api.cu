@@ -91,6 +91,7 @@ struct Layout {
   size_t b_segs = 0, b_q256 = 0, b_q128 = 0, b_fwdoff = 0, b_dqoff = 0, b_kgs = 0, b_kgsegs = 0, b_kt = 0,
          b_parts = 0, b_qbb = 0, b_kbb = 0;
   size_t keep = 0, keep_bytes = 0, qb_of = 0, kb_of = 0;
+  size_t tcls = 0;
   size_t f_cnt = 0, f_order = 0, f_ent = 0;
   size_t D = 0, lse2 = 0, q_cnt = 0, q_order = 0, q_ent = 0, k_ucnt = 0, k_order = 0, k_lcnt = 0, k_lsteps = 0,
          k_ent = 0;
@@ -323,6 +324,7 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     }
   }
   const size_t H = static_cast<size_t>(P.hm_count);
+  L.tcls = take(std::max<size_t>(1, H * P.dq_per_hm));
   if (fwd) {
     L.f_cnt = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
     L.f_order = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
@@ -589,7 +591,9 @@ lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     wl.n_sorted = static_cast<int>(n_rows);
     wl.expand = P.Hq / P.hm_count;
     int ph = phase_begin(0, c.st);
-    launch_plan_fwd(c.V, wl, c.st);
+    uint8_t* tcls = c.ws + c.L.tcls;
+    launch_classify(c.V, tcls, c.st);
+    launch_plan_fwd(c.V, tcls, wl, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
     AttnArgs a = base_args(c);
@@ -648,6 +652,10 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
   phase_end(ph, c.st);
   uint32_t* hist = reinterpret_cast<uint32_t*>(c.ws + c.L.hist);
   int* counters = reinterpret_cast<int*>(c.ws + c.L.counters);
+  uint8_t* tcls = c.ws + c.L.tcls;
+  ph = phase_begin(3, c.st);  // the tile classes serve both lists
+  launch_classify(c.V, tcls, c.st);
+  phase_end(ph, c.st);
   if (k_units > 0) {
     WorkList wl{};
     wl.cnt = reinterpret_cast<int*>(c.ws + c.L.k_ucnt);
@@ -660,7 +668,7 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     int* list_cnt = reinterpret_cast<int*>(c.ws + c.L.k_lcnt);
     int* list_steps = reinterpret_cast<int*>(c.ws + c.L.k_lsteps);
     ph = phase_begin(3, c.st);
-    launch_plan_dkv(c.V, wl, list_cnt, list_steps, c.st);
+    launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
     AttnArgs a = base_args(c);
@@ -690,7 +698,7 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     wl.n_sorted = static_cast<int>(q_rows);
     wl.expand = P.Hq / P.hm_count;
     ph = phase_begin(5, c.st);
-    launch_plan_dq(c.V, wl, c.st);
+    launch_plan_dq(c.V, tcls, wl, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
     AttnArgs a = base_args(c);

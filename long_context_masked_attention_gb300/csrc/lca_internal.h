@@ -48,9 +48,12 @@ struct WorkList {
 void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int* kb_bounds, uint32_t* keep,
                              int* qb_of, int* kb_of, const int* row_ptr, const int* col_idx, long long blk_nnz,
                              size_t keep_bytes, int* status, cudaStream_t st);
-void launch_plan_fwd(const PlanView& pv, const WorkList& wl, cudaStream_t st);
-void launch_plan_dq(const PlanView& pv, const WorkList& wl, cudaStream_t st);
-void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, int* list_steps, cudaStream_t st);
+// Class of every 128x128 tile, [map head][segment at dq_off][query tile][key tile] bytes.
+void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st);
+void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st);
+void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st);
+void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, int* list_cnt, int* list_steps,
+                     cudaStream_t st);
 void launch_sort(const WorkList& wl, cudaStream_t st);
 void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st);
 void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st);

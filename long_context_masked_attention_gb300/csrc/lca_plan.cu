@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "lca_internal.h"
 #include "sm103.cuh"
 
@@ -65,12 +67,45 @@ void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int
   }
 }
 
+// ---------------------------------------------------------------- tile classes
+// Every 128x128 tile (query tile qt, key tile kt) of every segment and map
+// head is classified once, one warp per tile, into a byte array laid out like
+// the dQ lists: [map head][segment at dq_off[s]][qt][kt].  The three list
+// builders below only compact this array.
+__global__ void classify_tiles_kernel(PlanView pv, uint8_t* __restrict__ tcls, long long total) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < total; w += warps) {
+    const int hm = static_cast<int>(w / pv.dq_per_hm);
+    const long long t = w % pv.dq_per_hm;
+    int lo = 0, hi = pv.n_seg;  // last segment whose offset is <= t (it holds t: empty ones share the next offset)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pv.dq_off[mid] <= t) lo = mid; else hi = mid;
+    }
+    const SegInfo sg = pv.segs[lo];
+    const long long r = t - pv.dq_off[lo];
+    const int qt = static_cast<int>(r / sg.nk), kt = static_cast<int>(r % sg.nk);
+    const uint32_t c = classify_tile_warp(pv.mask, sg, hm, qt * kTile, kt * kTile);
+    if (lane == 0) tcls[w] = static_cast<uint8_t>(c);
+  }
+}
+
+void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st) {
+  const long long total = static_cast<long long>(pv.hm_count) * pv.dq_per_hm;
+  if (total == 0) return;
+  note_launches(1);
+  const long long blocks = std::min<long long>((total + 7) / 8, 16384);
+  classify_tiles_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(pv, tcls, total);
+}
+
 // ---------------------------------------------------------------- query-major lists
-// One warp per list row (map head, segment, query block of SUB*128 rows).
+// One warp per list row (map head, segment, query block of SUB*128 rows); the
+// warp takes 32 key tiles at a time and places the non-empty ones with a ballot.
 // Entry = key tile index | class of sub-tile 0 << 24 | class of sub-tile 1 << 26.
 template <int SUB>
-__global__ void plan_q_rows_kernel(PlanView pv, int* __restrict__ cnt, uint32_t* __restrict__ entries,
-                                   uint32_t* __restrict__ hist) {
+__global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ cnt,
+                                   uint32_t* __restrict__ entries, uint32_t* __restrict__ hist) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int R = (SUB == 2) ? pv.R256 : pv.R128;
@@ -80,17 +115,23 @@ __global__ void plan_q_rows_kernel(PlanView pv, int* __restrict__ cnt, uint32_t*
   const int s = find_bucket(qstart, pv.n_seg, rr);
   const SegInfo sg = pv.segs[s];
   const int qb = rr - qstart[s];
+  const int nq = (sg.q_len + kTile - 1) / kTile;
   const long long per_hm = (SUB == 2) ? pv.fwd_per_hm : pv.dq_per_hm;
   const long long off = (SUB == 2) ? pv.fwd_off[s] : pv.dq_off[s];
   uint32_t* out = entries + hm * per_hm + off + static_cast<long long>(qb) * sg.nk;
+  const uint8_t* cls0 = tcls + hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(qb * SUB) * sg.nk;
+  const bool has1 = (SUB == 2) && (qb * SUB + 1 < nq);
   int n = 0;
-  for (int kt = 0; kt < sg.nk; ++kt) {
-    const uint32_t c0 = classify_tile_warp(pv.mask, sg, hm, qb * SUB * kTile, kt * kTile);
-    const uint32_t c1 = (SUB == 2) ? classify_tile_warp(pv.mask, sg, hm, qb * SUB * kTile + kTile, kt * kTile) : 0u;
-    if (c0 | c1) {
-      if (lane == 0) out[n] = static_cast<uint32_t>(kt) | (c0 << 24) | (c1 << 26);
-      ++n;
+  for (int k0 = 0; k0 < sg.nk; k0 += 32) {
+    const int kt = k0 + lane;
+    uint32_t c0 = 0, c1 = 0;
+    if (kt < sg.nk) {
+      c0 = cls0[kt];
+      if (has1) c1 = cls0[sg.nk + kt];
     }
+    const uint32_t keep = __ballot_sync(0xFFFFFFFFu, (c0 | c1) != 0);
+    if ((c0 | c1) != 0) out[n + __popc(keep & ((1u << lane) - 1u))] = static_cast<uint32_t>(kt) | (c0 << 24) | (c1 << 26);
+    n += __popc(keep);
   }
   if (lane == 0) {
     cnt[row] = n;
@@ -98,27 +139,29 @@ __global__ void plan_q_rows_kernel(PlanView pv, int* __restrict__ cnt, uint32_t*
   }
 }
 
-void launch_plan_fwd(const PlanView& pv, const WorkList& wl, cudaStream_t st) {
+void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st) {
   const int rows = pv.hm_count * pv.R256;
   if (rows == 0) return;
   note_launches(1);
-  plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, wl.cnt, static_cast<uint32_t*>(wl.entries), wl.hist);
+  plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, static_cast<uint32_t*>(wl.entries),
+                                                        wl.hist);
 }
 
-void launch_plan_dq(const PlanView& pv, const WorkList& wl, cudaStream_t st) {
+void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st) {
   const int rows = pv.hm_count * pv.R128;
   if (rows == 0) return;
   note_launches(1);
-  plan_q_rows_kernel<1><<<(rows + 7) / 8, 256, 0, st>>>(pv, wl.cnt, static_cast<uint32_t*>(wl.entries), wl.hist);
+  plan_q_rows_kernel<1><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, static_cast<uint32_t*>(wl.entries),
+                                                        wl.hist);
 }
 
 // ---------------------------------------------------------------- key-major lists
 // One warp per unit (map KV head gm, key group, key tile).  For a shared map
 // (H' = 1) the unit has one list; for per-head maps it has one list per query
 // head of the KV head.  Entry = {segment, query tile | class << 24}.
-__global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* __restrict__ list_cnt,
-                                     int* __restrict__ list_steps, int2* __restrict__ entries,
-                                     uint32_t* __restrict__ hist, int n_units) {
+__global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ ucnt,
+                                     int* __restrict__ list_cnt, int* __restrict__ list_steps,
+                                     int2* __restrict__ entries, uint32_t* __restrict__ hist, int n_units) {
   const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= n_units) return;
@@ -137,13 +180,18 @@ __global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* _
       const SegInfo sg = pv.segs[s];
       if (kt * kTile >= sg.k_len) continue;
       const int nq = (sg.q_len + kTile - 1) / kTile;
-      for (int qt = 0; qt < nq; ++qt) {
-        const uint32_t c = classify_tile_warp(pv.mask, sg, hm, qt * kTile, kt * kTile);
-        if (c) {
-          if (lane == 0) out[n] = make_int2(s, qt | static_cast<int>(c << 24));
-          ++n;
-          steps += (qt * kTile + 64 < sg.q_len) ? 2 : 1;  // 64-row halves inside the segment
+      const uint8_t* col = tcls + hm * pv.dq_per_hm + pv.dq_off[s] + kt;
+      for (int q0 = 0; q0 < nq; q0 += 32) {
+        const int qt = q0 + lane;
+        const uint32_t c = (qt < nq) ? col[static_cast<long long>(qt) * sg.nk] : 0u;
+        const uint32_t keep = __ballot_sync(0xFFFFFFFFu, c != 0);
+        int my_steps = 0;
+        if (c != 0) {
+          out[n + __popc(keep & ((1u << lane) - 1u))] = make_int2(s, qt | static_cast<int>(c << 24));
+          my_steps = (qt * kTile + 64 < sg.q_len) ? 2 : 1;  // 64-row halves inside the segment
         }
+        n += __popc(keep);
+        steps += __reduce_add_sync(0xFFFFFFFFu, my_steps);
       }
     }
     if (lane == 0) {
@@ -158,11 +206,12 @@ __global__ void plan_kv_units_kernel(PlanView pv, int* __restrict__ ucnt, int* _
   }
 }
 
-void launch_plan_dkv(const PlanView& pv, const WorkList& wl, int* list_cnt, int* list_steps, cudaStream_t st) {
+void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, int* list_cnt, int* list_steps,
+                     cudaStream_t st) {
   const int n_units = wl.n_sorted;
   if (n_units == 0) return;
   note_launches(1);
-  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, wl.cnt, list_cnt, list_steps,
+  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, list_cnt, list_steps,
                                                           static_cast<int2*>(wl.entries), wl.hist, n_units);
 }
 
