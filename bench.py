@@ -11,6 +11,17 @@ FLOPs: 4*d*nnz for the forward and 10*d*nnz for the backward, nnz = attended
 (query, key) cells summed over query heads, counted exactly on the device by
 lca_mask_nnz (checked against the oracle by the tests).
 
+Other workloads (--workload; each prints its own JSON line, with the same
+per-problem forward/backward breakdown; the default line above is the
+headline):
+  dense48k     sequence lengths 1K..48K at 48K tokens per step, MHA 64:64 and
+               GQA 64:8, CAUSAL and CAUSAL_DOC (70/30 document-length mixture)
+  blocksparse  32K/64K/128K tokens, MHA and GQA, uniform 64/128 blocks keeping
+               half of each block row (diagonal included) and variable blocks
+               U{32..256} keeping half of the block pairs
+  shards512k   524,288 tokens of Pareto(1.2) documents cut into U{1K..32K}
+               token shards, shuffled and packed into one launch, GQA 64:8
+
 Arms:
   default            the CUDA library; prints one JSON line (rank 0)
   --impl reference   the fp64 CPU oracle on the host cores, on a bounded sample
@@ -45,11 +56,69 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_problems(only=None):
-    from gen import STATIC_KINDS, config2
+WORKLOADS = {
+    "sweep8k": "static_mask_sweep_8k_gqa64x8_d128",
+    "dense48k": "dense_length_sweep_1k_48k_48k_tokens_mha64_gqa64x8_d128",
+    "blocksparse": "block_sparse_32k_64k_128k_mha64_gqa64x8_d128",
+    "shards512k": "shard_batch_512k_pareto_docs_gqa64x8_d128",
+}
 
-    kinds = [k for k in STATIC_KINDS if only is None or k in only.split(",")]
-    return [config2(k) for k in kinds]
+
+def workload_problems(only=None, workload="sweep8k"):
+    from gen import STATIC_KINDS, config2, config3, config4, config5
+
+    if workload == "dense48k":
+        probs = [config3(S * 1024, h, kind) for S in (1, 2, 4, 8, 16, 32, 48) for h in ("mha", "gqa")
+                 for kind in ("CAUSAL", "CAUSAL_DOC")]
+    elif workload == "blocksparse":
+        probs = [config4(S * 1024, h, var) for S in (32, 64, 128) for h in ("mha", "gqa")
+                 for var in ("uniform64", "uniform128", "variable")]
+    elif workload == "shards512k":
+        probs = [config5()]
+    else:
+        kinds = [k for k in STATIC_KINDS if only is None or k in only.split(",")]
+        return [config2(k) for k in kinds]
+    return [p for p in probs if only is None or p.name in only.split(",")]
+
+
+def time_problem(lca, p, ws, flush, steps, warmup, tensors=None):
+    """Median forward and backward milliseconds of one problem (L2 flushed
+    before every timed call pair), with its attended-cell count."""
+    import torch
+
+    from gen import make_tensors
+
+    dev = ws.device
+    q, k, v, do = tensors if tensors is not None else make_tensors(p, device=dev)
+    call = lca.marshal(p.Tq, p.Tk, p.Hq, p.Hkv, p.d, p.segments, p.mask, p.scale)
+    nnz = int(lca.mask_nnz(call).sum().item())
+    o = torch.empty_like(q)
+    lse = torch.empty((p.Hq, p.Tq), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for s in range(warmup + steps):
+        flush.zero_()
+        e = ev[s - warmup] if s >= warmup else None
+        if e:
+            e[0].record(stream)
+        lca.attn_fwd(q, k, v, p.segments, p.mask, p.scale, out=o, lse=lse, workspace=ws, call=call)
+        if e:
+            e[1].record(stream)
+        lca.attn_bwd(do, q, k, v, o, lse, p.segments, p.mask, p.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+                     call=call)
+        if e:
+            e[2].record(stream)
+    torch.cuda.synchronize()
+    st = lca.read_status(ws)
+    if st != (0, 0):
+        raise RuntimeError(f"device status after {p.name}: {st}")
+    f_ms = statistics.median(a.elapsed_time(b) for a, b, _ in ev)
+    b_ms = statistics.median(b.elapsed_time(c) for _, b, c in ev)
+    fl_f, fl_b = 4.0 * p.d * nnz, 10.0 * p.d * nnz
+    return {"nnz": nnz, "fwd_ms": f_ms, "bwd_ms": b_ms, "fwd_tflops": fl_f / (f_ms * 1e-3) / 1e12,
+            "bwd_tflops": fl_b / (b_ms * 1e-3) / 1e12,
+            "tflops": (fl_f + fl_b) / ((f_ms + b_ms) * 1e-3) / 1e12}
 
 
 # ------------------------------------------------------------------ clocks
@@ -228,6 +297,8 @@ def run_ours(args):
             dist.barrier()
 
     lca.load()
+    if args.workload != "sweep8k":
+        return run_workload(args, lca, dev, rank, world, barrier)
     probs = workload_problems(args.only)
     p0 = probs[0]
     q, k, v, do = make_tensors(p0, device=dev)
@@ -333,8 +404,8 @@ def run_ours(args):
                     "launches": n_launch, "peak_source": f"{pk_src} sustained bf16"}
     phase_ms = {ph: sum(v) / args.steps for ph, v in phases.items()}
     per_mask = {}
-    for p, n, ff, fb in zip(probs, nnz, f_fwd, f_bwd):
-        per_mask[p.mask.kind] = {"nnz": n}
+    for p in probs:
+        per_mask[p.mask.kind] = time_problem(lca, p, ws, flush, args.steps, 1, tensors=(q, k, v, do))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -345,13 +416,59 @@ def run_ours(args):
         "pct_of_peak": 100.0 * value / pk["bf16_tflops_sustained"],
         "peak_tflops": pk["bf16_tflops_sustained"], "peak_source": f"{pk_src} bf16 sustained",
         "roofline": roofline, "phase_ms_per_step": phase_ms, "gpu_launches": launches,
-        "clocks": clk, "e2e": e2e, "per_mask_nnz": per_mask,
+        "clocks": clk, "e2e": e2e, "per_mask": per_mask,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
             line["cpu_baseline"] = cpu_baseline()
         except Exception as exc:  # noqa: BLE001
             line["cpu_baseline"] = {"value": None, "error": str(exc)[:200]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_workload(args, lca, dev, rank, world, barrier):
+    """One JSON line for a non-default workload: every problem timed on its
+    own (fwd and bwd medians), value = all FLOPs / sum of per-problem times."""
+    import torch
+
+    probs = workload_problems(args.only, args.workload)
+    calls = [lca.marshal(p.Tq, p.Tk, p.Hq, p.Hkv, p.d, p.segments, p.mask, p.scale) for p in probs]
+    ws = torch.empty(max(lca.workspace_size(c, True) for c in calls), dtype=torch.uint8, device=dev)
+    del calls
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(dev.index or 0)
+    barrier()
+    clocks.start()
+    launches0 = lca.launch_count()
+    rows = {}
+    for p in probs:
+        rows[p.name] = time_problem(lca, p, ws, flush, args.steps, args.warmup)
+        torch.cuda.empty_cache()
+    launches = lca.launch_count() - launches0
+    clk = clocks.stop()
+    flops = sum(14.0 * 128 * r["nnz"] for r in rows.values())
+    ms = sum(r["fwd_ms"] + r["bwd_ms"] for r in rows.values())
+    tot_ms, tot_flops = aggregate(ms, flops, world, dev)
+    pk, pk_src = peaks()
+    value = tot_flops / (tot_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; seeded lengths and maps)",
+        "config": {"workload": WORKLOADS[args.workload], "problems": [p.name for p in probs], "head_dim": 128,
+                   "l2": "flushed before every timed forward+backward (256 MiB write)",
+                   "timing": "per problem: median of the timed steps; a step = every problem once",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_peak": 100.0 * value / pk["bf16_tflops_sustained"], "peak_tflops": pk["bf16_tflops_sustained"],
+        "peak_source": f"{pk_src} bf16 sustained", "gpu_launches": launches * world, "clocks": clk, "e2e": None,
+        "per_problem": rows,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -369,7 +486,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, help="comma-separated mask kinds (profiling runs; not a bench line)")
+    ap.add_argument("--only", default=None, help="comma-separated mask kinds or problem names (partial runs)")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep8k")
     ap.add_argument("--_oracle_sample", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args(argv)
     if args._oracle_sample is not None:
