@@ -59,6 +59,7 @@ void phase_end(int p, cudaStream_t st) {
 }
 
 constexpr size_t kAlign = 256;
+constexpr size_t kMaxPartialSlots = 256;  // 32 MiB of f32 dK/dV partial sums at most
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -95,6 +96,8 @@ struct Layout {
   size_t f_cnt = 0, f_order = 0, f_ent = 0;
   size_t D = 0, lse2 = 0, q_cnt = 0, q_order = 0, q_ent = 0, k_ucnt = 0, k_order = 0, k_lcnt = 0, k_lsteps = 0,
          k_ent = 0;
+  size_t k_usteps = 0, k_nchunk = 0, k_istart = 0, k_sstart = 0, k_nwork = 0, k_part = 0;
+  int k_max_slots = 0;
   size_t total = 0;
 };
 
@@ -342,6 +345,15 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     L.k_lcnt = take(sizeof(int) * std::max<size_t>(1, H * P.RK));
     L.k_lsteps = take(sizeof(int) * std::max<size_t>(1, H * P.RK));
     L.k_ent = take(sizeof(int2) * std::max<size_t>(1, H * P.dkv_per_hm));
+    const size_t n_units = std::max<size_t>(1, hkv_m * P.RK);
+    L.k_usteps = take(sizeof(int) * n_units);
+    L.k_nchunk = take(sizeof(int) * n_units);
+    L.k_istart = take(sizeof(int) * (n_units + 1));
+    L.k_sstart = take(sizeof(int) * n_units);
+    L.k_nwork = take(sizeof(int));
+    // partial-sum slots for chunks of split dK/dV units: [slot][dV, dK][128][128] f32
+    L.k_max_slots = static_cast<int>(std::min<size_t>(kMaxPartialSlots, n_units * (P.Hkv / hkv_m)));
+    L.k_part = take(sizeof(float) * 2 * kTile * kHeadDim * static_cast<size_t>(L.k_max_slots));
   }
   L.total = o;
   return L;
@@ -667,9 +679,17 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     wl.expand = P.Hkv / hkv_m;
     int* list_cnt = reinterpret_cast<int*>(c.ws + c.L.k_lcnt);
     int* list_steps = reinterpret_cast<int*>(c.ws + c.L.k_lsteps);
+    int* usteps = reinterpret_cast<int*>(c.ws + c.L.k_usteps);
+    DkvSplit sp{};
+    sp.nchunk = reinterpret_cast<int*>(c.ws + c.L.k_nchunk);
+    sp.item_start = reinterpret_cast<int*>(c.ws + c.L.k_istart);
+    sp.split_start = reinterpret_cast<int*>(c.ws + c.L.k_sstart);
+    sp.n_work = reinterpret_cast<int*>(c.ws + c.L.k_nwork);
+    sp.max_slots = c.L.k_max_slots;
     ph = phase_begin(3, c.st);
-    launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, c.st);
+    launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, c.st);
     launch_sort(wl, c.st);
+    launch_split_dkv(wl, usteps, sp, sms, c.st);
     phase_end(ph, c.st);
     AttnArgs a = base_args(c);
     a.cnt = wl.cnt;
@@ -679,13 +699,21 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     a.list_steps = list_steps;
     a.counter = wl.counter;
     a.expand = wl.expand;
-    a.n_work = static_cast<int>(k_units * wl.expand);
+    a.n_work = static_cast<int>(k_units * wl.expand + sp.max_slots);  // bound for the grid; the device holds the count
+    a.item_start = sp.item_start;
+    a.split_start = sp.split_start;
+    a.nchunk = sp.nchunk;
+    a.usteps = usteps;
+    a.n_work_dev = sp.n_work;
+    a.partials = reinterpret_cast<float*>(c.ws + c.L.k_part);
+    a.n_units = static_cast<int>(k_units);
     a.D = D;
     a.lse2 = lse2;
     a.dk = dk;
     a.dv = dv;
     ph = phase_begin(4, c.st);
     launch_bwd_dkv(tq64, tk, tv, tdo64, a, sms, c.st);
+    launch_dkv_reduce(a, c.st);
     phase_end(ph, c.st);
   }
   if (q_rows > 0) {

@@ -390,7 +390,9 @@ enum : int {
 
 struct Item {
   int valid, kg, kt, g, unit_hm, nsteps;  // unit_hm: first map head of the unit's lists
-  int rk, pad;
+  int rk;
+  int begin;  // first of the unit's steps this item runs (chunks of split units)
+  int slot;   // partial-sum slot of a chunk, -1 when the item writes dK/dV itself
 };
 
 // Per-step data the producer warp stages for the compute warps (buffer b of
@@ -427,6 +429,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
   uint32_t steps = 0;
   int kv_issued = 0;
   int it = 0;
+  const int n_work = *a.n_work_dev;
   for (;; ++it) {
     const int slot = it & 1;
     if (it >= 2 && !waitw(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 210)) goto abort;
@@ -436,24 +439,30 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       w = __shfl_sync(0xFFFFFFFFu, w, 0);
       Item inf;
       inf.valid = 0;
-      if (w < a.n_work) {
-        // consecutive items: the KV heads of one unit, so the cost order (longest first) holds across heads
-        const int unit = a.order[w / a.expand];
+      if (w < n_work) {
+        // sorted unit i holding item w; its items are chunk-major, then KV head, so the
+        // cost order (longest first) holds across heads and chunks
+        int lo = 0, hi = a.n_units;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (a.item_start[mid] <= w) lo = mid; else hi = mid;
+        }
+        const int unit = a.order[lo];
+        const int local = w - a.item_start[lo];
+        const int P = a.nchunk[unit];
+        const int c = local / a.expand;
         const int gm = unit / pv.RK, rk = unit % pv.RK;
         const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
         inf.valid = 1;
         inf.kg = kg;
         inf.kt = rk - pv.kt_start[kg];
         inf.rk = rk;
-        inf.g = (pv.hm_count == 1) ? (w % a.expand) : gm;
+        inf.g = (pv.hm_count == 1) ? (local % a.expand) : gm;
         inf.unit_hm = 0;
-        int n = 0;
-        if (pv.hm_count == 1) {
-          n = pv.G * a.list_steps[rk];
-        } else {
-          for (int l = 0; l < pv.G; ++l) n += a.list_steps[(inf.g * pv.G + l) * pv.RK + rk];
-        }
-        inf.nsteps = n;
+        const long long S = a.usteps[unit];
+        inf.begin = static_cast<int>(S * c / P);
+        inf.nsteps = static_cast<int>(S * (c + 1) / P) - inf.begin;
+        inf.slot = (P > 1) ? a.split_start[lo] + local : -1;
       }
       if (lane == 0) {
         items[slot] = inf;
@@ -471,12 +480,14 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         }
       }
       kv_issued = it + 1;
-      for (int l = 0; l < pv.G; ++l) {
+      int us = 0;  // steps of the unit walked so far (loads issued only for [begin, begin + nsteps))
+      const int us_end = inf.begin + inf.nsteps;
+      for (int l = 0; l < pv.G && us < us_end; ++l) {
         const int h = inf.g * pv.G + l;
         const int hm = (pv.hm_count == 1) ? 0 : h;
         const int n_in_list = a.list_cnt[hm * pv.RK + inf.rk];
         const long long ebase = hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(inf.kt) * grp.pairs;
-        for (int e0 = 0; e0 < n_in_list; e0 += 32) {
+        for (int e0 = 0; e0 < n_in_list && us < us_end; e0 += 32) {
           // lane-parallel fetch of up to 32 entries and their segments
           int2 en = make_int2(0, 0);
           SegInfo sgl{};
@@ -485,7 +496,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             sgl = pv.segs[en.x];
           }
           const int batch = min(32, n_in_list - e0);
-          for (int t = 0; t < batch; ++t) {
+          for (int t = 0; t < batch && us < us_end; ++t) {
             SegInfo sg;
             sg.q_off = __shfl_sync(0xFFFFFFFFu, sgl.q_off, t);
             sg.q_len = __shfl_sync(0xFFFFFFFFu, sgl.q_len, t);
@@ -501,6 +512,11 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             for (int half = 0; half < 2; ++half) {
               const int r0 = qt * kTile + 64 * half;
               if (r0 >= sg.q_len) continue;
+              if (us < inf.begin || us >= us_end) {  // outside this chunk
+                ++us;
+                continue;
+              }
+              ++us;
               const int b = steps % kRing;
               const uint32_t reuse = steps / kRing;  // how many times ring slot b was filled before
               if (reuse >= 1 && !waitw(&bar[B_MEMPTY + b], (reuse - 1) & 1, a, 213)) goto abort;
@@ -705,7 +721,27 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     const int jg = inf.kt * kTile + j;
     const bool valid = jg < grp.k_len;
     const size_t orow = (static_cast<size_t>(grp.k_off + (valid ? jg : 0)) * pv.Hkv + inf.g) * kHeadDim + half * 64;
-    if (inf.nsteps > 0) {
+    if (inf.nsteps > 0 && inf.slot >= 0) {  // chunk of a split unit: f32 partial sums, all 128 rows
+      if (!waitw(&bar[B_ACCFULL], acc_items & 1, a, 233)) return;
+      ++acc_items;
+      tc_fence_after();
+      float* pdv = a.partials + static_cast<size_t>(inf.slot) * (2 * kTile * kHeadDim) + j * kHeadDim + half * 64;
+      float* pdk = pdv + kTile * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + tl + 256 + half * 64 + 32 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(pdv + 32 * c + 4 * u) = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+        tmem_ld32(tbase + tl + 384 + half * 64 + 32 * c, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(pdk + 32 * c + 4 * u) = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+      }
+    } else if (inf.nsteps > 0) {
       if (!waitw(&bar[B_ACCFULL], acc_items & 1, a, 233)) return;
       ++acc_items;
       tc_fence_after();
@@ -785,6 +821,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One block per (sorted unit, KV head of the unit); blocks of units that were
+// not split return at once.
+__global__ void __launch_bounds__(256) reduce_kernel(const AttnArgs a) {
+  const int i = blockIdx.x / a.expand, gi = blockIdx.x % a.expand;
+  const int unit = a.order[i];
+  const int P = a.nchunk[unit];
+  if (P <= 1) return;
+  const PlanView& pv = a.pv;
+  const int gm = unit / pv.RK, rk = unit % pv.RK;
+  const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
+  const KeyGroup grp = pv.kgs[kg];
+  const int kt = rk - pv.kt_start[kg];
+  const int g = (pv.hm_count == 1) ? gi : gm;
+  __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(a.dk);
+  __nv_bfloat16* dV = static_cast<__nv_bfloat16*>(a.dv);
+  for (int idx = threadIdx.x; idx < kTile * (kHeadDim / 4); idx += blockDim.x) {
+    const int j = idx / (kHeadDim / 4), d4 = 4 * (idx % (kHeadDim / 4));
+    const int jg = kt * kTile + j;
+    if (jg >= grp.k_len) continue;
+    float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), sk = sv;
+    for (int c = 0; c < P; ++c) {
+      const float* base = a.partials + static_cast<size_t>(a.split_start[i] + c * a.expand + gi) * (2 * kTile * kHeadDim);
+      const float4 v = *reinterpret_cast<const float4*>(base + j * kHeadDim + d4);
+      const float4 k = *reinterpret_cast<const float4*>(base + kTile * kHeadDim + j * kHeadDim + d4);
+      sv.x += v.x; sv.y += v.y; sv.z += v.z; sv.w += v.w;
+      sk.x += k.x; sk.y += k.y; sk.z += k.z; sk.w += k.w;
+    }
+    const size_t row = (static_cast<size_t>(grp.k_off + jg) * pv.Hkv + g) * kHeadDim + d4;
+    *reinterpret_cast<uint2*>(dV + row) = make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w));
+    *reinterpret_cast<uint2*>(dK + row) =
+        make_uint2(pack_bf16x2(sk.x * a.scale, sk.y * a.scale), pack_bf16x2(sk.z * a.scale, sk.w * a.scale));
+  }
+}
+
 }  // namespace dkv
 }  // namespace
 
@@ -807,9 +877,17 @@ void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensor
     cudaFuncSetAttribute(dkv::dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
     configured = true;
   }
+  // the item count is known on the device only (split pass); surplus CTAs find no work and exit
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
   dkv::dkv_kernel<<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+}
+
+void launch_dkv_reduce(const AttnArgs& a, cudaStream_t st) {
+  const long long blocks = static_cast<long long>(a.n_units) * a.expand;
+  if (blocks == 0) return;
+  note_launches(1);
+  dkv::reduce_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(a);
 }
 
 }  // namespace lca

@@ -53,7 +53,16 @@ void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st);
 void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st);
 void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st);
 void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, int* list_cnt, int* list_steps,
-                     cudaStream_t st);
+                     int* usteps, cudaStream_t st);
+// Chunk counts, item and partial-slot prefixes over the cost-sorted units.
+struct DkvSplit {
+  int* nchunk;
+  int* item_start;
+  int* split_start;
+  int* n_work;
+  int max_slots;
+};
+void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st);
 void launch_sort(const WorkList& wl, cudaStream_t st);
 void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st);
 void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st);
@@ -74,6 +83,15 @@ struct AttnArgs {
   int* counter;
   int n_work;
   int expand;
+  // dK/dV: units longer than a share of the per-SM load are cut into chunks of
+  // 64-row steps; a chunk writes f32 partial dV, dK that a reduction sums.
+  const int* item_start;   // [n_units + 1] first work item of each sorted unit
+  const int* split_start;  // [n_units] first partial slot of each sorted unit
+  const int* nchunk;       // [unit] chunks of each of the unit's items (1 = whole)
+  const int* usteps;       // [unit] 64-row steps of each of the unit's items
+  const int* n_work_dev;   // work items, written on the device by the split pass
+  float* partials;         // [slot][dV, dK][128 rows][128] f32
+  int n_units;
   int* status;
   unsigned long long wait_limit_ns;
   float scale;       // softmax scale
@@ -94,5 +112,7 @@ void launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const AttnArgs& a, int num_sms, cudaStream_t st);
 void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                     const AttnArgs& a, int num_sms, cudaStream_t st);
+// Sums the partial dV, dK of split units into the bf16 outputs.
+void launch_dkv_reduce(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace lca

@@ -161,7 +161,8 @@ void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl,
 // head of the KV head.  Entry = {segment, query tile | class << 24}.
 __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ ucnt,
                                      int* __restrict__ list_cnt, int* __restrict__ list_steps,
-                                     int2* __restrict__ entries, uint32_t* __restrict__ hist, int n_units) {
+                                     int* __restrict__ usteps, int2* __restrict__ entries,
+                                     uint32_t* __restrict__ hist, int n_units) {
   const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= n_units) return;
@@ -170,7 +171,7 @@ __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tc
   const KeyGroup grp = pv.kgs[kg];
   const int kt = rk - pv.kt_start[kg];
   const int nlists = (pv.hm_count == 1) ? 1 : pv.G;
-  int cost = 0;
+  int cost = 0, unit_steps = 0;
   for (int l = 0; l < nlists; ++l) {
     const int hm = (pv.hm_count == 1) ? 0 : gm * pv.G + l;
     int2* out = entries + hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(kt) * grp.pairs;
@@ -199,20 +200,120 @@ __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tc
       list_steps[hm * pv.RK + rk] = steps;
     }
     cost += n;
+    unit_steps += steps;
   }
   if (lane == 0) {
     ucnt[unit] = cost;
+    // one work item covers all G query heads of a KV head; a shared map is one list used G times
+    usteps[unit] = (pv.hm_count == 1) ? pv.G * unit_steps : unit_steps;
     atomicAdd(hist + min(cost, kCostBuckets - 1), 1u);
   }
 }
 
 void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, int* list_cnt, int* list_steps,
-                     cudaStream_t st) {
+                     int* usteps, cudaStream_t st) {
   const int n_units = wl.n_sorted;
   if (n_units == 0) return;
   note_launches(1);
-  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, list_cnt, list_steps,
+  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, list_cnt, list_steps, usteps,
                                                           static_cast<int2*>(wl.entries), wl.hist, n_units);
+}
+
+// ---------------------------------------------------------------- dK/dV split
+// One block.  A unit whose items are longer than 3/4 of the average per-SM
+// load (and than kMinChunkSteps) is cut into equal chunks of steps, so that a
+// few very long key tiles (keys every query attends, as with global tokens)
+// do not set the kernel's length.  Chunks of one item write partial sums to
+// their own slots; if the slots would run out, chunks grow until they fit.
+constexpr int kMinChunkSteps = 64;
+
+__device__ __forceinline__ long long block_sum_ll(long long v, long long* red) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  __syncthreads();
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  long long t = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
+// Exclusive block scan of one int per thread; returns the prefix and the block total.
+__device__ __forceinline__ int block_scan_excl(int v, int* red, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();
+  if (lane == 31) red[wid] = incl;
+  __syncthreads();
+  int before = 0;
+  total = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+    if (w < wid) before += red[w];
+    total += red[w];
+  }
+  return before + incl - v;
+}
+
+__global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__ order, const int* __restrict__ usteps,
+                                                         int n_units, int expand, int num_sms, int max_slots,
+                                                         int* __restrict__ nchunk, int* __restrict__ item_start,
+                                                         int* __restrict__ split_start, int* __restrict__ n_work) {
+  __shared__ long long red_ll[32];
+  __shared__ int red[32];
+  long long local = 0;
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) local += usteps[u];
+  const long long total = block_sum_ll(local, red_ll) * expand;
+  long long target = total * 3 / (4LL * max(1, num_sms));
+  if (target < kMinChunkSteps) target = kMinChunkSteps;
+  for (int round = 0; round < 40; ++round) {  // grow chunks until the partial slots suffice
+    long long slots = 0;
+    for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
+      const long long c = (usteps[u] + target - 1) / target;
+      if (c > 1) slots += c * expand;
+    }
+    if (block_sum_ll(slots, red_ll) <= max_slots) break;
+    target *= 2;
+  }
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
+    const long long c = (usteps[u] + target - 1) / target;
+    nchunk[u] = static_cast<int>(c > 1 ? c : 1);
+  }
+  __syncthreads();
+  int item_base = 0, slot_base = 0;
+  for (int i0 = 0; i0 < n_units; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    int ni = 0, si = 0;
+    if (i < n_units) {
+      const int c = nchunk[order[i]];
+      ni = c * expand;
+      si = (c > 1) ? ni : 0;
+    }
+    int tot_i, tot_s;
+    const int pi = block_scan_excl(ni, red, tot_i);
+    const int ps = block_scan_excl(si, red, tot_s);
+    if (i < n_units) {
+      item_start[i] = item_base + pi;
+      split_start[i] = slot_base + ps;
+    }
+    item_base += tot_i;
+    slot_base += tot_s;
+  }
+  if (threadIdx.x == 0) {
+    item_start[n_units] = item_base;
+    *n_work = item_base;
+  }
+}
+
+void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st) {
+  note_launches(1);
+  split_dkv_kernel<<<1, 1024, 0, st>>>(wl.order, usteps, wl.n_sorted, wl.expand, num_sms, sp.max_slots, sp.nchunk,
+                                       sp.item_start, sp.split_start, sp.n_work);
 }
 
 // ---------------------------------------------------------------- cost sort

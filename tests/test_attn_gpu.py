@@ -91,3 +91,40 @@ def test_bounded_wait_reports_timeout(lca):
     assert code == 5 and where == 900
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum()) == 8.0
+
+
+def _split_cases():
+    """Layouts where some dK/dV units are far longer than the per-SM share,
+    so the planner cuts them into chunks whose partial sums are reduced:
+    keys every query attends (global tokens), every unit long (FULL with all
+    query heads on one KV head), per-head block maps, one long document."""
+    from gen import MaskSpec, Problem, Segment
+
+    out = [
+        cases.single(2048, "GLOBAL_SLIDING", 8, 1, 128, 41, num_global=16, window_left=100, window_right=100),
+        cases.single(1024, "FULL", 8, 1, 128, 42),
+        cases.block_uniform(1536, 128, Hq=4, Hkv=1, d=128, seed=43),
+        cases.docs([1800, 150, 98], "CAUSAL_DOC", 8, 2, 128, 44),
+        Problem("q_gt_k", 1500, 700, 8, 1, 128, [Segment(0, 1500, 0, 700)], MaskSpec("FULL"), 45),
+    ]
+    for p in out:
+        p.name = "split_" + p.name
+    return out
+
+
+SPLIT = _split_cases()
+
+
+@pytest.mark.parametrize("prob", SPLIT, ids=[p.name for p in SPLIT])
+def test_split_dkv_parity(lca, prob):
+    _parity(lca, prob)
+
+
+def test_split_dkv_deterministic(lca):
+    prob = SPLIT[0]
+    q, k, v, do = make_tensors(prob)
+    o, lse = run_fwd(lca, prob, q, k, v)
+    g1 = run_bwd(lca, prob, q, k, v, do, o, lse)
+    g2 = run_bwd(lca, prob, q, k, v, do, o, lse)
+    for a, b in zip(g1, g2):
+        assert np.array_equal(to_np(a), to_np(b))
