@@ -121,6 +121,35 @@ def time_problem(lca, p, ws, flush, steps, warmup, tensors=None):
             "tflops": (fl_f + fl_b) / ((f_ms + b_ms) * 1e-3) / 1e12}
 
 
+# ------------------------------------------------------------------ measured traffic
+TRAFFIC_PROFILES = {"dkv": "profiles/dkv_kernel_traffic_sweep8k_gqa64x8.md"}
+
+
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from its committed ncu summary, or None
+    when there is none or the kernel's sources changed since the capture."""
+    import hashlib
+    import re
+
+    rel = TRAFFIC_PROFILES.get(kernel)
+    if rel is None or not os.path.exists(os.path.join(ROOT, rel)):
+        return None
+    text = open(os.path.join(ROOT, rel)).read()
+    b = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    srcs = re.search(r"kernel_sources:\s*(.+)", text)
+    sha = re.search(r"kernel_sources_sha256:\s*([0-9a-f]{64})", text)
+    if not (b and srcs and sha):
+        return None
+    h = hashlib.sha256()
+    for f in srcs.group(1).split():
+        path = os.path.join(ROOT, "long_context_masked_attention_gb300", "csrc", f)
+        if not os.path.exists(path):
+            return None
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    return float(b.group(1)) if h.hexdigest() == sha.group(1) else None
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -400,7 +429,8 @@ def run_ours(args):
         flops_dom = alg[dom] * d * sum(nnz) * args.steps
         achieved = flops_dom / (sum(phases[dom]) * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
-                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"], "traffic": None,
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
+                    "traffic": measured_traffic(dom), "traffic_unit": "bytes per launch (ncu, cold L2)",
                     "launches": n_launch, "peak_source": f"{pk_src} sustained bf16"}
     phase_ms = {ph: sum(v) / args.steps for ph, v in phases.items()}
     per_mask = {}
