@@ -138,6 +138,27 @@ LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, 
                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Merge of partial forward results ("长上下文能力：FlashAttention vs.
+ * RingAttention", Blockwise Parallel Transformer and RingAttention sections:
+ * attention over a union of disjoint key blocks is assembled from each
+ * block's output and softmax normaliser).  Part p holds o_parts[p] (device
+ * bf16 [Tq][Hq][d]) and lse_parts[p] (device float [Hq][Tq], natural log) for
+ * the same queries over a key set disjoint from every other part's, e.g. one
+ * lca_attn_fwd call per key chunk.  Writes
+ *     lse[h][i] = log sum_p exp(lse_p[h][i])
+ *     o[i][h]   = sum_p exp(lse_p[h][i] - lse[h][i]) * o_p[i][h]   (bf16)
+ * and o = 0, lse = -inf for rows no part attends (every lse_p = -inf).
+ * A causal mask split into key chunks is a FULL call for the chunks below the
+ * diagonal plus a CAUSAL call whose segments pair each query chunk with its
+ * own, equally long key chunk.
+ * o_parts, lse_parts: HOST arrays of n_parts device pointers,
+ * 1 <= n_parts <= LCA_MERGE_MAX_PARTS; o may alias o_parts[0] and lse
+ * lse_parts[0].  d must be 128; o pointers 16-byte aligned, lse pointers
+ * 4-byte aligned.  Asynchronous on `stream`; needs no workspace. */
+#define LCA_MERGE_MAX_PARTS 16
+LCA_API lca_status lca_attn_merge(const void* const* o_parts, const float* const* lse_parts, int32_t n_parts, void* o,
+                                  float* lse, int32_t Tq, int32_t Hq, int32_t d, void* stream);
+
 /* Test hook: writes the mask of one segment and query head, evaluated by the
  * same device predicate the attention kernels apply, as bytes (1 = attend)
  * into `out` (device, q_len*k_len, row-major). */

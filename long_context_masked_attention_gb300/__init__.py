@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     Mask,
     attn_bwd,
     attn_fwd,
+    attn_merge,
     load,
     marshal,
     mask_materialize,

@@ -25,7 +25,8 @@ STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "L
           4: "LCA_ERR_CUDA", 5: "LCA_ERR_TIMEOUT", 6: "LCA_ERR_DEVICE_ARG"}
 EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
             "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
-            "lca_last_error_detail", "lca_attn_fwd_static_workspace", "lca_status_string", "lca_version")
+            "lca_last_error_detail", "lca_attn_fwd_static_workspace", "lca_status_string", "lca_version",
+            "lca_attn_merge")
 PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
 
 
@@ -242,6 +243,25 @@ def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=N
     _check(load().lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                                C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(), workspace.numel(),
                                _stream(stream)), "lca_attn_fwd")
+    return out, lse
+
+
+def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
+    """Merges forward results of the same queries over disjoint key sets:
+    o_parts [Tq,Hq,128] bf16 and lse_parts [Hq,Tq] f32 CUDA tensors ->
+    (o, lse).  `out`/`lse` may be part 0's tensors."""
+    import torch
+
+    n = len(o_parts)
+    if n != len(lse_parts):
+        raise ValueError("o_parts and lse_parts differ in length")
+    Tq, Hq, d = o_parts[0].shape
+    out = torch.empty_like(o_parts[0]) if out is None else out
+    lse = torch.empty_like(lse_parts[0]) if lse is None else lse
+    optrs = (C.c_void_p * n)(*[t.data_ptr() for t in o_parts])
+    lptrs = (C.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
+    _check(load().lca_attn_merge(optrs, lptrs, n, C.c_void_p(out.data_ptr()), C.c_void_p(lse.data_ptr()), Tq, Hq, d,
+                                 _stream(stream)), "lca_attn_merge")
     return out, lse
 
 

@@ -630,6 +630,31 @@ lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   return LCA_OK;
 }
 
+lca_status lca_attn_merge(const void* const* o_parts, const float* const* lse_parts, int32_t n_parts, void* o,
+                          float* lse, int32_t Tq, int32_t Hq, int32_t d, void* stream) {
+  if (d != kHeadDim) return LCA_ERR_UNSUPPORTED;
+  if (n_parts < 1 || n_parts > LCA_MERGE_MAX_PARTS || Tq < 0 || Hq <= 0 || !o_parts || !lse_parts)
+    return LCA_ERR_INVALID_ARG;
+  if (static_cast<long long>(Tq) * Hq * 16 / 256 >= 0x7FFFFFFFLL) return LCA_ERR_UNSUPPORTED;  // grid size
+  if (Tq == 0) return LCA_OK;
+  if (!o || !aligned16(o) || !lse || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return LCA_ERR_INVALID_ARG;
+  MergeArgs m{};
+  for (int p = 0; p < n_parts; ++p) {
+    if (!o_parts[p] || !aligned16(o_parts[p]) || !lse_parts[p] || (reinterpret_cast<uintptr_t>(lse_parts[p]) & 3u) != 0)
+      return LCA_ERR_INVALID_ARG;
+    m.o[p] = o_parts[p];
+    m.lse[p] = lse_parts[p];
+  }
+  m.n = n_parts;
+  m.out = o;
+  m.lse_out = lse;
+  m.Tq = Tq;
+  m.Hq = Hq;
+  launch_merge(m, static_cast<cudaStream_t>(stream));
+  LCA_CUDA(cudaGetLastError());
+  return LCA_OK;
+}
+
 lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream) {

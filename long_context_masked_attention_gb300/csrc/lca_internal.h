@@ -67,6 +67,15 @@ void launch_sort(const WorkList& wl, cudaStream_t st);
 void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st);
 void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st);
 void launch_nnz(const PlanView& pv, int max_q_len, unsigned long long* acc, unsigned long long* nnz, cudaStream_t st);
+struct MergeArgs {
+  const void* o[16];
+  const float* lse[16];
+  int n;
+  void* out;
+  float* lse_out;
+  int Tq, Hq;
+};
+void launch_merge(const MergeArgs& m, cudaStream_t st);
 void launch_d_prepass(const void* o, const void* dout, const float* lse, float* D, float* lse2, int Tq, int Hq,
                       cudaStream_t st);
 void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream_t st);

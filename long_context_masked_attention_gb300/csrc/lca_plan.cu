@@ -535,6 +535,59 @@ void launch_d_prepass(const void* o, const void* dout, const float* lse, float* 
                                          Tq, Hq);
 }
 
+// ---------------------------------------------------------------- partial merge
+// Half a warp per (row, head): 16 lanes x 8 bf16 = one 256-byte output row.
+__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs m) {
+  const long long gid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long rh = gid >> 4;  // row * Hq + head
+  const int sub = threadIdx.x & 15;
+  if (rh >= static_cast<long long>(m.Tq) * m.Hq) return;
+  const int row = static_cast<int>(rh / m.Hq), h = static_cast<int>(rh % m.Hq);
+  const size_t li = static_cast<size_t>(h) * m.Tq + row;
+  float lp[16];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    lp[p] = (p < m.n) ? m.lse[p][li] : -INFINITY;
+    mx = fmaxf(mx, lp[p]);
+  }
+  uint4* out = static_cast<uint4*>(m.out) + rh * 16 + sub;
+  if (mx == -INFINITY) {  // no part attends this row
+    *out = make_uint4(0, 0, 0, 0);
+    if (sub == 0) m.lse_out[li] = -INFINITY;
+    return;
+  }
+  float w[16], sum = 0.f;
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    w[p] = (lp[p] == -INFINITY) ? 0.f : expf(lp[p] - mx);
+    sum += w[p];
+  }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    if (w[p] == 0.f) continue;
+    const uint4 v = static_cast<const uint4*>(m.o[p])[rh * 16 + sub];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      acc[2 * c] += w[p] * __uint_as_float(u[c] << 16);
+      acc[2 * c + 1] += w[p] * __uint_as_float(u[c] & 0xFFFF0000u);
+    }
+  }
+  const float inv = 1.f / sum;
+  *out = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                    pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+  if (sub == 0) m.lse_out[li] = mx + logf(sum);
+}
+
+void launch_merge(const MergeArgs& m, cudaStream_t st) {
+  const long long threads = static_cast<long long>(m.Tq) * m.Hq * 16;
+  if (threads == 0) return;
+  note_launches(1);
+  merge_kernel<<<static_cast<int>((threads + 255) / 256), 256, 0, st>>>(m);
+}
+
 __global__ void fill_lse_kernel(float* lse, int Tq, int Hq, int row0, int nrows) {
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(nrows) * Hq) return;

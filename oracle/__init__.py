@@ -20,6 +20,7 @@ Parity status: every function here is pinned by tests/test_oracle_*.py
 constructions, finite differences and an independent library cross-check).
 """
 from .masks import segment_mask, mask_row_counts, dense_mask  # noqa: F401
+from .merge import merge_partials  # noqa: F401
 from .attention import (  # noqa: F401
     attention_forward,
     attention_backward,

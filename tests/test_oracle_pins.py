@@ -373,3 +373,44 @@ def test_row_local_helpers_match_full_backward(prob):
                 dV2[seg.k_off:seg.k_off + seg.k_len, h // G] += b
     np.testing.assert_allclose(dK2, dK, atol=1e-12)
     np.testing.assert_allclose(dV2, dV, atol=1e-12)
+
+
+# ---------------------------------------------------------------- partial merge
+def _partition_forward(rng, nq=37, nk=50, d=8, parts=3, causal=False):
+    q, k, v = (rng.standard_normal((n, d)) for n in (nq, nk, nk))
+    mask = rng.random((nq, nk)) < 0.6
+    if causal:
+        mask &= np.tril(np.ones((nq, nk), dtype=bool), nk - nq)
+    mask[3] = False  # a row that attends nothing
+    owner = rng.integers(0, parts, nk)  # key j belongs to part owner[j]
+    owner[: parts] = np.arange(parts)
+    full = oracle.segment_head_forward(q, k, v, mask, 0.3)
+    pieces = [oracle.segment_head_forward(q, k, v, mask & (owner == p)[None, :], 0.3) for p in range(parts)]
+    return full, pieces
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("parts", [1, 2, 5])
+def test_merge_of_a_key_partition_is_the_union(parts, causal):
+    """Softmax over a union of disjoint key sets from each set's output and
+    log-normaliser (exact up to rounding); rows empty in some parts, and a
+    row empty in all, included."""
+    rng = np.random.Generator(np.random.PCG64(200 + parts + 10 * causal))
+    (o_full, l_full, _), pieces = _partition_forward(rng, parts=parts, causal=causal)
+    o, l = oracle.merge_partials([p[0][:, None, :] for p in pieces], [p[1][None, :] for p in pieces])
+    assert np.array_equal(np.isneginf(l[0]), np.isneginf(l_full))
+    fin = np.isfinite(l_full)
+    np.testing.assert_allclose(l[0][fin], l_full[fin], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(o[:, 0], o_full, rtol=0, atol=1e-12)
+    assert np.all(o[3, 0] == 0.0) and np.isneginf(l[0, 3])
+
+
+def test_merge_worked_example():
+    """Two parts of one row, by hand: keys {a} with score 0 and value 1, keys
+    {b, c} with scores ln 2, ln 2 and values 4, 7.  Union: weights 1, 2, 2 over
+    5 -> O = (1 + 8 + 14) / 5 = 4.6, LSE = ln 5.  Part 1: O = 1, LSE = 0;
+    part 2: O = 5.5, LSE = ln 4."""
+    o, l = oracle.merge_partials([np.array([[[1.0]]]), np.array([[[5.5]]])],
+                                 [np.array([[0.0]]), np.array([[np.log(4.0)]])])
+    assert o[0, 0, 0] == pytest.approx(4.6, abs=1e-12)
+    assert l[0, 0] == pytest.approx(np.log(5.0), abs=1e-12)

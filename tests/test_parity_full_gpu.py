@@ -183,3 +183,32 @@ def test_shard_batch_512k(lca):
     o, lse = outputs[0], outputs[1]
     assert float((o[ridx].float() - o_doc.float()).abs().max()) <= 1e-2
     assert float((lse[:, ridx] - lse_doc).abs().max()) <= 1e-3
+
+
+def test_split_key_tile_full_size_global_sliding(lca):
+    """8K global-sliding sweep case, GQA 64:8: key tile 0 holds the 64 global
+    keys every query attends, so its dK/dV units are far longer than the rest
+    and run as chunks whose f32 partials are reduced.  That tile's dK/dV (KV
+    head 0, all 8192 rows of its 8 query heads) is checked exactly."""
+    from gen import config2
+
+    prob = config2("GLOBAL_SLIDING")
+    inputs, outputs = _run(lca, prob)
+    _check_rows(lca, prob, inputs, outputs, _heads(prob))
+    _check_gradient_sums(prob, inputs, outputs)
+    q, k, v, do = inputs
+    _, _, _, dk, dv = outputs
+    G = prob.Hq // prob.Hkv
+    cols = np.arange(128)
+    dK_ref = np.zeros((128, prob.d))
+    dV_ref = np.zeros((128, prob.d))
+    seg = prob.segments[0]
+    for h in range(G):
+        for r0 in range(0, seg.q_len, 2048):
+            rows = np.arange(r0, min(seg.q_len, r0 + 2048))
+            a, b = oracle.key_grads_from_rows(prob, q, k, v, do, 0, h, rows, cols)
+            dK_ref += a
+            dV_ref += b
+    for name, x, r in (("dK", to_np(dk[cols, 0]), dK_ref), ("dV", to_np(dv[cols, 0]), dV_ref)):
+        rel = np.linalg.norm(x - r) / max(np.linalg.norm(r), 1e-30)
+        assert rel <= BWD_REL_L2, (name, rel)
