@@ -159,6 +159,37 @@ LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, 
 LCA_API lca_status lca_attn_merge(const void* const* o_parts, const float* const* lse_parts, int32_t n_parts, void* o,
                                   float* lse, int32_t Tq, int32_t Hq, int32_t d, void* stream);
 
+/* Core-attention disaggregation planner ("Efficient Long-context Language
+ * Model Training by Core Attention Disaggregation": core attention is cut
+ * into token-level tasks that attention servers rebatch to balance compute).
+ * Host only; no CUDA call.  Cuts documents of lengths doc_len[0..n_docs) into
+ * query shards and assigns them to n_servers so that the causal attention
+ * work per server -- the cells (b(b+1) - a(a+1))/2 of each of its shards
+ * [a, b) -- is balanced:
+ *   1. each document is cut into equal pieces no longer than max_shard
+ *      (0 = no limit; else max_shard >= 2 * min_shard);
+ *   2. pieces go to the least-loaded server, most expensive first;
+ *   3. while the most loaded server exceeds the mean by more than
+ *      `tolerance` (relative), its most expensive piece at least 2*min_shard
+ *      long is cut where its cells halve, and step 2 is redone.
+ * Shard [a, b) of a document whose keys start at position s is the segment
+ * {q_off: its place in the server's packed query buffer, q_len: b - a,
+ *  k_off: s, k_len: b} of a CAUSAL call: it attends keys [s, s + b).
+ * Shards come out ordered by server, then document, then start.  Up to
+ * max_shards entries are written to `shards` (host) and the count to
+ * n_shards; server_cells (host, n_servers entries, may be NULL) receives each
+ * server's cells per head.  LCA_ERR_WORKSPACE if max_shards is too small
+ * (n_shards then holds the count needed). */
+typedef struct {
+  int32_t doc;    /* document index                        */
+  int32_t start;  /* first query token, document-relative  */
+  int32_t len;    /* query tokens                          */
+  int32_t server; /* attention server it is assigned to    */
+} lca_cad_shard;
+LCA_API lca_status lca_cad_plan(const int32_t* doc_len, int32_t n_docs, int32_t n_servers, int32_t min_shard,
+                                int32_t max_shard, double tolerance, lca_cad_shard* shards, int32_t max_shards,
+                                int32_t* n_shards, int64_t* server_cells);
+
 /* Test hook: writes the mask of one segment and query head, evaluated by the
  * same device predicate the attention kernels apply, as bytes (1 = attend)
  * into `out` (device, q_len*k_len, row-major). */

@@ -11,6 +11,8 @@ from .binding import (  # noqa: F401
     attn_bwd,
     attn_fwd,
     attn_merge,
+    cad_plan,
+    CadPlan,
     load,
     marshal,
     mask_materialize,

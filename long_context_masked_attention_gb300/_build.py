@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblca_attn.so")
-SOURCES = ["lca_api.cu", "lca_plan.cu", "lca_fwd.cu", "lca_bwd.cu"]
+SOURCES = ["lca_api.cu", "lca_plan.cu", "lca_fwd.cu", "lca_bwd.cu", "lca_cad.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 
@@ -38,7 +38,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
         if force or _stale(o, s):
             jobs.append([nv, *ARCH, *FLAGS, "-c", s, "-o", o])
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
@@ -47,7 +47,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 sys.stderr.write(res.stdout + res.stderr)
             if res.returncode != 0:
                 raise RuntimeError("nvcc failed: " + " ".join(cmd))
-    objs = [os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    objs = [os.path.join(BUILD, os.path.splitext(s)[0] + ".o") for s in SOURCES]
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + ".tmp"
         res = subprocess.run([nv, *ARCH, "-shared", "-o", tmp, *objs, "-lrt", "-ldl", "-lpthread"],

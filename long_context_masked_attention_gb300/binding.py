@@ -26,7 +26,7 @@ STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "L
 EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
             "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
             "lca_last_error_detail", "lca_attn_fwd_static_workspace", "lca_status_string", "lca_version",
-            "lca_attn_merge")
+            "lca_attn_merge", "lca_cad_plan")
 PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
 
 
@@ -244,6 +244,51 @@ def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=N
                                C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(), workspace.numel(),
                                _stream(stream)), "lca_attn_fwd")
     return out, lse
+
+
+class CadShard_t(C.Structure):
+    _fields_ = [("doc", C.c_int32), ("start", C.c_int32), ("len", C.c_int32), ("server", C.c_int32)]
+
+
+@dataclass
+class CadPlan:
+    """Shards (doc, start, len, server) ordered by server then document, and
+    each server's causal attention cells per head."""
+    shards: list
+    server_cells: list
+
+    def server_batch(self, server: int, doc_lengths):
+        """The server's packed query batch: CAUSAL segments (q_off, q_len,
+        k_off, k_len) over keys packed in document order, and for each packed
+        query row its row in the document-ordered token buffer."""
+        starts = np.concatenate([[0], np.cumsum(np.asarray(doc_lengths, dtype=np.int64))])
+        segs, rows, q = [], [], 0
+        for doc, start, n, srv in self.shards:
+            if srv != server:
+                continue
+            segs.append((q, n, int(starts[doc]), start + n))
+            rows.append(np.arange(starts[doc] + start, starts[doc] + start + n))
+            q += n
+        return segs, (np.concatenate(rows) if rows else np.zeros(0, dtype=np.int64))
+
+
+def cad_plan(doc_lengths, n_servers, min_shard=1024, max_shard=32768, tolerance=0.05) -> CadPlan:
+    """Core-attention disaggregation plan (host only, lca_cad_plan)."""
+    arr, ptr = _i32(doc_lengths)
+    n = C.c_int32(0)
+    cells = (C.c_int64 * max(1, int(n_servers)))()
+    cap = max(16, 4 * len(arr) + 4 * int(n_servers))
+    while True:
+        buf = (CadShard_t * cap)()
+        code = load().lca_cad_plan(ptr, len(arr), int(n_servers), int(min_shard), int(max_shard),
+                                   C.c_double(float(tolerance)), buf, cap, C.byref(n), cells)
+        if code == 3 and n.value > cap:  # LCA_ERR_WORKSPACE: more shards than room
+            cap = n.value
+            continue
+        _check(code, "lca_cad_plan")
+        break
+    shards = [(buf[i].doc, buf[i].start, buf[i].len, buf[i].server) for i in range(n.value)]
+    return CadPlan(shards, [int(cells[i]) for i in range(int(n_servers))])
 
 
 def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
