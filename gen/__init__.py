@@ -37,6 +37,7 @@ MASK_KINDS = (
     "BLOCK_CAUSAL_DOC",
     "BLOCK_SPARSE_UNIFORM",
     "BLOCK_SPARSE_VARIABLE",
+    "FLASHMASK",
 )
 STATIC_KINDS = MASK_KINDS[:12]
 KIND_ID = {k: i for i, k in enumerate(MASK_KINDS)}
@@ -73,6 +74,7 @@ class MaskSpec:
     heads_in_map: int = 1
     blk_row_ptr: np.ndarray | None = None  # int32 [heads_in_map * n_qb + 1]
     blk_col_idx: np.ndarray | None = None  # int32 [nnz blocks], sorted per row
+    col_bounds: np.ndarray | None = None  # FLASHMASK: int32 [Tk, 4] {lts, lte, uts, ute}
 
     def n_qb(self, Tq: int) -> int:
         if self.kind == "BLOCK_SPARSE_UNIFORM":

@@ -82,7 +82,10 @@ typedef enum {
   LCA_MASK_PREFIX_LM_DOC = 10,   /* j < seg_prefix[segment] or j <= ie                 */
   LCA_MASK_BLOCK_CAUSAL_DOC = 11,/* floor(j/block) <= floor(ie/block)                  */
   LCA_MASK_BLOCK_SPARSE_UNIFORM = 12,  /* keep[h][qb][kb], blocks q_block x kv_block  */
-  LCA_MASK_BLOCK_SPARSE_VARIABLE = 13  /* keep[h][qb][kb], blocks from qb/kb_bounds    */
+  LCA_MASK_BLOCK_SPARSE_VARIABLE = 13, /* keep[h][qb][kb], blocks from qb/kb_bounds   */
+  LCA_MASK_FLASHMASK = 14  /* column-wise (FlashMask, named by the LongCA-bench review as
+                              covering every family): key j (global position) is masked
+                              for segment rows [lts_j, lte_j) U [uts_j, ute_j)            */
 } lca_mask_kind;
 
 typedef struct {
@@ -110,6 +113,10 @@ typedef struct {
   const int32_t* blk_row_ptr; /* device [heads_in_map*n_qb+1]: CSR row starts      */
   const int32_t* blk_col_idx; /* device [blk_nnz]: kept kv block indices           */
   int64_t blk_nnz;
+  /* FLASHMASK: device int32 [Tk][4] = {lts, lte, uts, ute} per global key
+   * position, rows relative to the query segment reading that key; 16-byte
+   * aligned.  One map for all heads. */
+  const int32_t* col_bounds;
 } lca_mask_desc;
 
 typedef struct {

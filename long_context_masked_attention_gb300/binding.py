@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "liblca_attn.so")
 MASK_KINDS = (
     "FULL", "CAUSAL", "SLIDING", "CAUSAL_SLIDING", "DOC", "CAUSAL_DOC", "SHARED_QUESTION", "GLOBAL_SLIDING",
     "CAUSAL_BLOCKWISE", "PREFIX_LM_CAUSAL", "PREFIX_LM_DOC", "BLOCK_CAUSAL_DOC", "BLOCK_SPARSE_UNIFORM",
-    "BLOCK_SPARSE_VARIABLE",
+    "BLOCK_SPARSE_VARIABLE", "FLASHMASK",
 )
 STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "LCA_ERR_WORKSPACE",
           4: "LCA_ERR_CUDA", 5: "LCA_ERR_TIMEOUT", 6: "LCA_ERR_DEVICE_ARG"}
@@ -56,6 +56,7 @@ class MaskDesc_t(C.Structure):
         ("heads_in_map", C.c_int32),
         ("blk_row_ptr", C.c_void_p), ("blk_col_idx", C.c_void_p),
         ("blk_nnz", C.c_int64),
+        ("col_bounds", C.c_void_p),
     ]
 
 
@@ -123,6 +124,7 @@ class Mask:
     heads_in_map: int = 1
     blk_row_ptr: object = None
     blk_col_idx: object = None
+    col_bounds: object = None  # FLASHMASK: int32 [Tk, 4] {lts, lte, uts, ute}
 
 
 @dataclass
@@ -193,6 +195,13 @@ def marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale=0.0, device=None) -> Call:
         md.blk_row_ptr = trp.data_ptr()
         md.blk_col_idx = tci.data_ptr() if tci.numel() else None
         md.blk_nnz = int(tci.numel())
+    cb = getattr(mask, "col_bounds", None)
+    if cb is not None:
+        dev = device if device is not None else torch.device("cuda")
+        tcb = (cb.to(device=dev, dtype=torch.int32) if isinstance(cb, torch.Tensor)
+               else torch.from_numpy(np.ascontiguousarray(np.asarray(cb, dtype=np.int32))).to(dev)).contiguous()
+        keep.append(tcb)
+        md.col_bounds = tcb.data_ptr()
     return Call(shape, md, keep)
 
 

@@ -109,7 +109,7 @@ lca_status validate(const lca_shape* sh, const lca_mask_desc* md, HostPlan& P) {
   if (sh->n_seg > 0 && !sh->segs) return LCA_ERR_INVALID_ARG;
   if (!(std::isfinite(sh->scale)) || sh->scale < 0.f) return LCA_ERR_INVALID_ARG;
   if (static_cast<long long>(sh->Hq) * kHeadDim > (1LL << 30)) return LCA_ERR_UNSUPPORTED;
-  if (md->kind < LCA_MASK_FULL || md->kind > LCA_MASK_BLOCK_SPARSE_VARIABLE) return LCA_ERR_INVALID_ARG;
+  if (md->kind < LCA_MASK_FULL || md->kind > LCA_MASK_FLASHMASK) return LCA_ERR_INVALID_ARG;
   P.Tq = sh->Tq;
   P.Tk = sh->Tk;
   P.Hq = sh->Hq;
@@ -235,6 +235,11 @@ lca_status validate(const lca_shape* sh, const lca_mask_desc* md, HostPlan& P) {
     case LCA_MASK_CAUSAL_BLOCKWISE:
     case LCA_MASK_BLOCK_CAUSAL_DOC:
       if (m.block < 1) return LCA_ERR_INVALID_ARG;
+      break;
+    case LCA_MASK_FLASHMASK:
+      if (P.Tk > 0 && (!md->col_bounds || (reinterpret_cast<uintptr_t>(md->col_bounds) & 15u) != 0))
+        return LCA_ERR_INVALID_ARG;
+      m.cols = reinterpret_cast<const int4*>(md->col_bounds);
       break;
     case LCA_MASK_SHARED_QUESTION: {
       const int n = md->n_part_bounds;

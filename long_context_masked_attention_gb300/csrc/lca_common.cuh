@@ -32,6 +32,7 @@ enum MaskKind : int {
   kBlockCausalDoc = 11,
   kBlockSparseUniform = 12,
   kBlockSparseVariable = 13,
+  kFlashMask = 14,
 };
 
 enum TileClass : uint32_t { kTileEmpty = 0, kTileFull = 1, kTilePartial = 2 };
@@ -70,6 +71,7 @@ struct MaskCtx {
   const int* kb_of;       // variable: key block of each global key [Tk]
   const int* kb_start;    // variable: key block bounds [n_kb + 1]
   const int* qb_start;    // variable: query block bounds [n_qb + 1]
+  const int4* cols;       // FlashMask: {lts, lte, uts, ute} per global key [Tk]
 };
 
 __host__ __device__ __forceinline__ bool is_block_sparse(int kind) {
@@ -235,10 +237,34 @@ __device__ __forceinline__ uint32_t block_chunk_bits(const MaskCtx& m, const Seg
   return bits & range_bits(0, sg.k_len, j0);
 }
 
+// ---------------------------------------------------------------- FlashMask
+// Column-wise form: key column j masks the segment rows [lts, lte) U [uts, ute).
+__device__ __forceinline__ bool col_masks_row(const int4& b, int i) {
+  return (b.x <= i && i < b.y) || (b.z <= i && i < b.w);
+}
+
+__device__ __forceinline__ uint32_t flashmask_chunk_bits(const MaskCtx& m, const SegInfo& sg, int i, int j0) {
+  if (i < 0 || i >= sg.q_len || j0 >= sg.k_len) return 0u;
+  const int n = min(32, sg.k_len - j0);
+  const int4* c = m.cols + sg.k_off + j0;
+  uint32_t bits = 0u;
+  for (int t = 0; t < n; ++t) bits |= col_masks_row(__ldg(c + t), i) ? 0u : (1u << t);
+  return bits;
+}
+
+// Rows of [r0, r1) that column bounds b mask.
+__device__ __forceinline__ int col_masked_rows(const int4& b, int r0, int r1) {
+  const int n0 = max(0, min(b.y, r1) - max(b.x, r0));
+  const int n1 = max(0, min(b.w, r1) - max(b.z, r0));
+  const int both = max(0, min(min(b.y, b.w), r1) - max(max(b.x, b.z), r0));
+  return n0 + n1 - both;
+}
+
 // The mask predicate: bit t of the result is set iff query row i of the
 // segment attends key j0 + t (segment-relative), for query head map index hm.
 __device__ __forceinline__ uint32_t mask_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
   if (is_block_sparse(m.kind)) return block_chunk_bits(m, sg, hm, i, j0);
+  if (m.kind == kFlashMask) return flashmask_chunk_bits(m, sg, i, j0);
   return span_bits(row_span(m, sg, i), j0);
 }
 
@@ -260,6 +286,12 @@ __device__ __forceinline__ uint32_t classify_tile_warp(const MaskCtx& m, const S
       const bool kept = block_kept(m, hm, qbA + t / nk, kbA + t % nk);
       any |= kept;
       all &= kept;
+    }
+  } else if (m.kind == kFlashMask) {
+    for (int c = c0 + lane; c < c1; c += 32) {
+      const int masked = col_masked_rows(__ldg(m.cols + sg.k_off + c), r0, r1);
+      any |= masked < r1 - r0;
+      all &= masked == 0;
     }
   } else {
     for (int r = r0 + lane; r < r1; r += 32) {

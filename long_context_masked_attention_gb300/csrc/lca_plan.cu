@@ -401,13 +401,19 @@ __global__ void tile_classes_kernel(PlanView pv, int seg, int hm, uint8_t* __res
   if ((threadIdx.x & 31) == 0) out[tile] = static_cast<uint8_t>(c);
 }
 
-// nnz: interval families — one thread per query row, grid.y = segment.
+// nnz: interval families and FlashMask — one thread per query row, grid.y = segment.
 __global__ void nnz_rows_kernel(PlanView pv, unsigned long long* acc) {
   const int s = blockIdx.y;
   const SegInfo sg = pv.segs[s];
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   unsigned long long n = 0;
-  if (i < sg.q_len) n = static_cast<unsigned long long>(span_count(row_span(pv.mask, sg, i)));
+  if (i < sg.q_len) {
+    if (pv.mask.kind == kFlashMask) {
+      for (int j0 = 0; j0 < sg.k_len; j0 += 32) n += __popc(flashmask_chunk_bits(pv.mask, sg, i, j0));
+    } else {
+      n = static_cast<unsigned long long>(span_count(row_span(pv.mask, sg, i)));
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
   if ((threadIdx.x & 31) == 0 && n) atomicAdd(acc, n);

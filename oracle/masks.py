@@ -79,6 +79,13 @@ def segment_mask(spec, seg_index: int, seg, head: int = 0, rows=None) -> np.ndar
         m = (j < p) | (j <= ie)
     elif kind == "BLOCK_CAUSAL_DOC":
         m = (j // spec.block) <= (ie // spec.block)
+    elif kind == "FLASHMASK":
+        # column-wise form (FlashMask, named by the LongCA-bench review): key
+        # column j of the segment (global position k_off + j) is hidden from
+        # the segment rows [lts, lte) and [uts, ute)
+        cb = np.asarray(spec.col_bounds)[seg.k_off + j[0]]
+        lts, lte, uts, ute = (cb[:, t][None, :] for t in range(4))
+        m = ~(((i >= lts) & (i < lte)) | ((i >= uts) & (i < ute)))
     elif kind in ("BLOCK_SPARSE_UNIFORM", "BLOCK_SPARSE_VARIABLE"):
         q_pos = seg.q_off + i[:, 0]
         k_pos = seg.k_off + j[0]

@@ -67,6 +67,14 @@ def _segment_block(spec, s_index, seg, head):
                 C[r0:r0 + b, c0:c0 + b] = True
     elif kind in ("BLOCK_SPARSE_UNIFORM", "BLOCK_SPARSE_VARIABLE"):
         return _block_sparse_segment(spec, seg, head)
+    elif kind == "FLASHMASK":
+        out = np.ones((q, k), dtype=bool)
+        for jj in range(k):
+            lts, lte, uts, ute = (int(x) for x in spec.col_bounds[seg.k_off + jj])
+            for r in range(q):
+                if lts <= r < lte or uts <= r < ute:
+                    out[r, jj] = False
+        return out
     else:
         raise ValueError(kind)
     if q <= k:

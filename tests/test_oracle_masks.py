@@ -41,3 +41,33 @@ def test_block_sparse_generators_small(variant):
         counts = oracle.mask_row_counts(p, h)
         # half of the blocks of every block row are kept
         assert 0.3 < counts.sum() / (p.Tq * p.Tk) < 0.7
+
+
+# ---------------------------------------------------------------- FlashMask form
+FM_CASES = (cases.tiny_all(S=16)[:12] + cases.tiny_all(S=37)[:12]
+            + [p for p in cases.edge_cases(d=8) if p.name in ("edge_q_gt_k", "edge_tile_plus1")])
+
+
+@pytest.mark.parametrize("prob", FM_CASES, ids=[f"{p.name}_{i}" for i, p in enumerate(FM_CASES)])
+def test_flashmask_form_equals_family(prob):
+    """Each static family written in FlashMask's column form (test input)
+    gives, through the oracle's column predicate, the family's own mask, and
+    the brute-force column fill agrees cell by cell."""
+    from tests.flashmask_inputs import as_flashmask
+
+    fm = as_flashmask(prob)
+    want = oracle.dense_mask(prob)
+    assert np.array_equal(oracle.dense_mask(fm), want)
+    assert np.array_equal(brute_dense_mask(fm), want)
+
+
+def test_flashmask_worked_example():
+    """Hand-set columns of one 4x4 segment: key 0 hides no row; key 1 hides
+    row 0; key 2 hides rows 0-1 and 3; key 3 hides rows 1-2.  Rows read
+    keys {0,3}, {0,1}, {0,1,2}, {0,1,3}."""
+    from gen import MaskSpec, Problem, Segment
+
+    cb = np.array([[0, 0, 0, 0], [0, 1, 0, 0], [0, 2, 3, 4], [1, 3, 0, 0]], dtype=np.int32)
+    p = Problem("fm4", 4, 4, 1, 1, 8, [Segment(0, 4, 0, 4)], MaskSpec("FLASHMASK", col_bounds=cb), 1)
+    want = np.array([[1, 0, 0, 1], [1, 1, 0, 0], [1, 1, 1, 0], [1, 1, 0, 1]], dtype=bool)
+    assert np.array_equal(oracle.dense_mask(p), want)
