@@ -225,6 +225,7 @@ abort:
   mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
 }
 
+template <bool kCols>
 __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
@@ -276,7 +277,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       if (cls == kTilePartial) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t bits = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
+          const uint32_t bits = mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
 #pragma unroll
           for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
         }
@@ -325,6 +326,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   }
 }
 
+template <bool kCols>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
-    compute(a, sm, bar, items, tbase);
+    compute<kCols>(a, sm, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -420,6 +422,7 @@ __device__ __forceinline__ StepMeta* stat_meta(uint8_t* sm, int b) {
 // Steps of an item: for each query head of the KV head, each entry of its
 // list, each 64-row half of the 128-row query tile that lies inside the
 // segment.
+template <bool kCols>
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
                                          Item* items) {
@@ -539,7 +542,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                   const int wd = lane * 8 + u;  // word = query row * 4 + key chunk
-                  sw[wd] = mask_bits(pv.mask, sg, hm, r0 + (wd >> 2), inf.kt * kTile + 32 * (wd & 3));
+                  sw[wd] = mask_bits<kCols>(pv.mask, sg, hm, r0 + (wd >> 2), inf.kt * kTile + 32 * (wd & 3));
                 }
               }
               if (lane == 0) stat_meta(sm, b)->cls = static_cast<int>(cls);
@@ -778,6 +781,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   }
 }
 
+template <bool kCols>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
@@ -807,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   if (warp == 9) {
-    producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
+    producer<kCols>(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
@@ -862,25 +866,33 @@ void launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const AttnArgs& a, int num_sms, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(dq::dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
     configured = true;
   }
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
-  dq::dq_kernel<<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  if (a.pv.mask.kind == kFlashMask)
+    dq::dq_kernel<true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else
+    dq::dq_kernel<false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
 }
 
 void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                     const AttnArgs& a, int num_sms, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(dkv::dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
     configured = true;
   }
   // the item count is known on the device only (split pass); surplus CTAs find no work and exit
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
-  dkv::dkv_kernel<<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  if (a.pv.mask.kind == kFlashMask)
+    dkv::dkv_kernel<true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else
+    dkv::dkv_kernel<false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
 }
 
 void launch_dkv_reduce(const AttnArgs& a, cudaStream_t st) {

@@ -262,10 +262,22 @@ __device__ __forceinline__ int col_masked_rows(const int4& b, int r0, int r1) {
 
 // The mask predicate: bit t of the result is set iff query row i of the
 // segment attends key j0 + t (segment-relative), for query head map index hm.
+// kCols selects the FlashMask column form at compile time: the attention
+// kernels are instantiated twice so that the column loop never enlarges the
+// code the interval and block families run (a branch on the kind, even
+// never taken and not inlined, slowed the dK/dV producer measurably).
+template <bool kCols>
 __device__ __forceinline__ uint32_t mask_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
-  if (is_block_sparse(m.kind)) return block_chunk_bits(m, sg, hm, i, j0);
-  if (m.kind == kFlashMask) return flashmask_chunk_bits(m, sg, i, j0);
-  return span_bits(row_span(m, sg, i), j0);
+  if constexpr (kCols) {
+    return flashmask_chunk_bits(m, sg, i, j0);
+  } else {
+    if (is_block_sparse(m.kind)) return block_chunk_bits(m, sg, hm, i, j0);
+    return span_bits(row_span(m, sg, i), j0);
+  }
+}
+// Any family, chosen at run time (planning and test kernels).
+__device__ __forceinline__ uint32_t mask_bits_any(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
+  return (m.kind == kFlashMask) ? mask_bits<true>(m, sg, hm, i, j0) : mask_bits<false>(m, sg, hm, i, j0);
 }
 
 // Class of the 128x128 tile with rows [r0, r0+128) and keys [c0, c0+128) of

@@ -308,6 +308,7 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], 
   return f2lo(t) + f2hi(t);
 }
 
+template <bool kCols>
 __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
@@ -343,7 +344,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       uint32_t mb[4] = {~0u, ~0u, ~0u, ~0u};
       if (cls == kTilePartial) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mb[c] = mask_bits(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
+        for (int c = 0; c < 4; ++c) mb[c] = mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
       }
       if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
       ++s_cons;
@@ -420,6 +421,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
   }
 }
 
+template <bool kCols>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
@@ -460,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sQ, sKV, bar, items, tbase);
   } else {
-    softmax_wg(a, warp >> 2, bar, items, tbase);
+    softmax_wg<kCols>(a, warp >> 2, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -476,12 +478,16 @@ void launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap&
                 cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     configured = true;
   }
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
-  fwd_kernel<<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  if (a.pv.mask.kind == kFlashMask)
+    fwd_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  else
+    fwd_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
 }
 
 }  // namespace lca

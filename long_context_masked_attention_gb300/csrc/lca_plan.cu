@@ -382,7 +382,7 @@ __global__ void materialize_seg_kernel(PlanView pv, int seg, int hm, uint8_t* __
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int i = static_cast<int>(idx / nch);
     const int c = static_cast<int>(idx % nch);
-    const uint32_t bits = mask_bits(pv.mask, sg, hm, i, c * 32);
+    const uint32_t bits = mask_bits_any(pv.mask, sg, hm, i, c * 32);
     uint8_t* row = out + static_cast<long long>(i) * sg.k_len;
     for (int t = 0; t < 32; ++t) {
       const int j = c * 32 + t;
