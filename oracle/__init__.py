@@ -21,6 +21,7 @@ constructions, finite differences and an independent library cross-check).
 """
 from .masks import segment_mask, mask_row_counts, dense_mask  # noqa: F401
 from .merge import merge_partials  # noqa: F401
+from .dropout import philox4x32_10, keep_mask, keep_scale, drop_threshold  # noqa: F401
 from .attention import (  # noqa: F401
     attention_forward,
     attention_backward,

@@ -17,11 +17,18 @@ dK and dV of a KV head are summed over the query heads that share it
 over every segment that reads that key.  Masked cells have P = dS = 0.
 
 Head h reads KV head h // (Hq // Hkv).
+
+Dropout (FlashAttention review page, FlashAttention-1 核心优化, 算子融合):
+with `dropout` = (seed, p), the forward uses P~ = P * Z / k (Z from
+``oracle.dropout``) in O = P~ V, LSE stays that of P, and the backward is
+    dP~ = dO V^T,  D_i = sum_j P~_ij dP~_ij = dO_i . O_i,
+    dS = P * (Z/k * dP~ - D),  dV = P~^T dO,  dQ, dK as above.
 """
 from __future__ import annotations
 
 import numpy as np
 
+from .dropout import scaled_keep
 from .masks import segment_mask
 
 
@@ -31,8 +38,10 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def segment_head_forward(q_s, k_s, v_s, mask, scale):
-    """One segment, one head.  q_s [n_q, d], k_s/v_s [n_k, d], mask [n_q, n_k]."""
+def segment_head_forward(q_s, k_s, v_s, mask, scale, zk=None):
+    """One segment, one head.  q_s [n_q, d], k_s/v_s [n_k, d], mask [n_q, n_k];
+    zk [n_q, n_k] = Z / k of dropout, or None.  Returns O, LSE and P (the
+    undropped probabilities)."""
     s = scale * (q_s @ k_s.T)
     s = np.where(mask, s, -np.inf)
     has = mask.any(axis=1)
@@ -41,21 +50,23 @@ def segment_head_forward(q_s, k_s, v_s, mask, scale):
     l = e.sum(axis=1)
     lse = np.where(has, m + np.log(np.where(has, l, 1.0)), -np.inf)
     p = np.where(mask, np.exp(s - np.where(has, lse, 0.0)[:, None]), 0.0)
-    o = p @ v_s
+    o = (p if zk is None else p * zk) @ v_s
     return o, lse, p
 
 
-def segment_head_backward(q_s, k_s, v_s, do_s, mask, scale):
+def segment_head_backward(q_s, k_s, v_s, do_s, mask, scale, zk=None):
     """Returns dq_s, dk_s, dv_s, D (and O) for one segment and one head."""
-    o, lse, p = segment_head_forward(q_s, k_s, v_s, mask, scale)
-    dp = do_s @ v_s.T
-    D = (p * dp).sum(axis=1)
+    o, lse, p = segment_head_forward(q_s, k_s, v_s, mask, scale, zk)
+    pt = p if zk is None else p * zk  # the probabilities O was made from
+    dpt = do_s @ v_s.T
+    D = (pt * dpt).sum(axis=1)
     # the identity D_i = dO_i . O_i (FlashAttention-2's row statistic)
     assert np.allclose(D, (do_s * o).sum(axis=1), rtol=1e-9, atol=1e-9 * (1 + np.abs(D).max(initial=0)))
+    dp = dpt if zk is None else zk * dpt
     ds = p * (dp - D[:, None])
     dq = scale * (ds @ k_s)
     dk = scale * (ds.T @ q_s)
-    dv = p.T @ do_s
+    dv = pt.T @ do_s
     return dq, dk, dv, D, o, lse
 
 
@@ -63,9 +74,18 @@ def _kv_head(prob, h):
     return h // (prob.Hq // prob.Hkv)
 
 
-def attention_forward(prob, q, k, v, heads=None):
+def _zk(dropout, seg, h, rows=None):
+    """Z / k of segment `seg`'s rows (segment-relative; all when None) and
+    all of its keys, or None without dropout."""
+    if dropout is None:
+        return None
+    rows = np.arange(seg.q_len) if rows is None else np.asarray(rows)
+    return scaled_keep(dropout, h, seg.q_off + rows, np.arange(seg.k_len))
+
+
+def attention_forward(prob, q, k, v, heads=None, dropout=None):
     """Full forward.  Returns O [Tq, Hq, d] and LSE [Hq, Tq] (fp64); rows of
-    heads not in `heads` are left at 0 / -inf."""
+    heads not in `heads` are left at 0 / -inf.  `dropout` = (seed, p)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     scale = prob.softmax_scale
     O = np.zeros((prob.Tq, prob.Hq, prob.d))
@@ -76,13 +96,13 @@ def attention_forward(prob, q, k, v, heads=None):
             qs = slice(seg.q_off, seg.q_off + seg.q_len)
             ks = slice(seg.k_off, seg.k_off + seg.k_len)
             mask = segment_mask(prob.mask, s, seg, h)
-            o, lse, _ = segment_head_forward(q[qs, h], k[ks, g], v[ks, g], mask, scale)
+            o, lse, _ = segment_head_forward(q[qs, h], k[ks, g], v[ks, g], mask, scale, _zk(dropout, seg, h))
             O[qs, h] = o
             LSE[h, qs] = lse
     return O, LSE
 
 
-def attention_backward(prob, q, k, v, do, heads=None):
+def attention_backward(prob, q, k, v, do, heads=None, dropout=None):
     """Full backward.  Returns dQ [Tq, Hq, d], dK/dV [Tk, Hkv, d] (fp64).
     With `heads`, only those query heads contribute (dK/dV of a KV head are
     complete only when all of its query heads are listed)."""
@@ -97,14 +117,16 @@ def attention_backward(prob, q, k, v, do, heads=None):
             qs = slice(seg.q_off, seg.q_off + seg.q_len)
             ks = slice(seg.k_off, seg.k_off + seg.k_len)
             mask = segment_mask(prob.mask, s, seg, h)
-            dq, dk, dv, _, _, _ = segment_head_backward(q[qs, h], k[ks, g], v[ks, g], do[qs, h], mask, scale)
+            dq, dk, dv, _, _, _ = segment_head_backward(
+                q[qs, h], k[ks, g], v[ks, g], do[qs, h], mask, scale, _zk(dropout, seg, h)
+            )
             dQ[qs, h] = dq
             dK[ks, g] += dk
             dV[ks, g] += dv
     return dQ, dK, dV
 
 
-def forward_rows(prob, q, k, v, seg_index, head, rows):
+def forward_rows(prob, q, k, v, seg_index, head, rows, dropout=None):
     """Forward for selected rows (segment-relative) of one segment and head:
     returns O [len(rows), d], LSE [len(rows)]."""
     seg = prob.segments[seg_index]
@@ -115,11 +137,11 @@ def forward_rows(prob, q, k, v, seg_index, head, rows):
     kk = _f64(k[seg.k_off:seg.k_off + seg.k_len, g])
     vv = _f64(v[seg.k_off:seg.k_off + seg.k_len, g])
     mask = segment_mask(prob.mask, seg_index, seg, head, rows)
-    o, lse, _ = segment_head_forward(qr, kk, vv, mask, scale)
+    o, lse, _ = segment_head_forward(qr, kk, vv, mask, scale, _zk(dropout, seg, head, rows))
     return o, lse
 
 
-def backward_rows(prob, q, k, v, do, seg_index, head, rows):
+def backward_rows(prob, q, k, v, do, seg_index, head, rows, dropout=None):
     """dQ for selected rows (segment-relative) of one segment and head: a
     row's softmax, D_i and dS_ij depend on that row alone."""
     seg = prob.segments[seg_index]
@@ -131,11 +153,11 @@ def backward_rows(prob, q, k, v, do, seg_index, head, rows):
     kk = _f64(k[seg.k_off:seg.k_off + seg.k_len, g])
     vv = _f64(v[seg.k_off:seg.k_off + seg.k_len, g])
     mask = segment_mask(prob.mask, seg_index, seg, head, rows)
-    dq, _, _, _, _, _ = segment_head_backward(qr, kk, vv, dor, mask, scale)
+    dq, _, _, _, _, _ = segment_head_backward(qr, kk, vv, dor, mask, scale, _zk(dropout, seg, head, rows))
     return dq
 
 
-def key_grads_from_rows(prob, q, k, v, do, seg_index, head, rows, key_cols):
+def key_grads_from_rows(prob, q, k, v, do, seg_index, head, rows, key_cols, dropout=None):
     """Contribution of the given query rows of one segment and head to dK and
     dV of the given key columns (segment-relative): dK_j = tau sum_i dS_ij q_i,
     dV_j = sum_i P_ij dO_i over the listed rows only."""
@@ -149,8 +171,11 @@ def key_grads_from_rows(prob, q, k, v, do, seg_index, head, rows, key_cols):
     kk = _f64(k[seg.k_off:seg.k_off + seg.k_len, g])
     vv = _f64(v[seg.k_off:seg.k_off + seg.k_len, g])
     mask = segment_mask(prob.mask, seg_index, seg, head, rows)
+    zk = _zk(dropout, seg, head, rows)
     _, _, p = segment_head_forward(qr, kk, vv, mask, scale)
-    dp = dor @ vv.T
-    D = (p * dp).sum(axis=1)
+    pt = p if zk is None else p * zk
+    dpt = dor @ vv.T
+    D = (pt * dpt).sum(axis=1)
+    dp = dpt if zk is None else zk * dpt
     ds = p * (dp - D[:, None])
-    return scale * (ds[:, key_cols].T @ qr), p[:, key_cols].T @ dor
+    return scale * (ds[:, key_cols].T @ qr), pt[:, key_cols].T @ dor
