@@ -21,6 +21,8 @@ headline):
                U{32..256} keeping half of the block pairs
   shards512k   524,288 tokens of Pareto(1.2) documents cut into U{1K..32K}
                token shards, shuffled and packed into one launch, GQA 64:8
+  sweep8k_dropout  the 8K static-mask sweep with attention dropout p = 0.1
+               fused into the forward and backward kernels
 
 Arms:
   default            the CUDA library; prints one JSON line (rank 0)
@@ -61,7 +63,9 @@ WORKLOADS = {
     "dense48k": "dense_length_sweep_1k_48k_48k_tokens_mha64_gqa64x8_d128",
     "blocksparse": "block_sparse_32k_64k_128k_mha64_gqa64x8_d128",
     "shards512k": "shard_batch_512k_pareto_docs_gqa64x8_d128",
+    "sweep8k_dropout": "static_mask_sweep_8k_gqa64x8_d128_dropout0.1",
 }
+DROPOUT = {"sweep8k_dropout": (0x5EED, 0.1)}
 
 
 def workload_problems(only=None, workload="sweep8k"):
@@ -75,13 +79,13 @@ def workload_problems(only=None, workload="sweep8k"):
                  for var in ("uniform64", "uniform128", "variable")]
     elif workload == "shards512k":
         probs = [config5()]
-    else:
+    else:  # sweep8k, sweep8k_dropout
         kinds = [k for k in STATIC_KINDS if only is None or k in only.split(",")]
         return [config2(k) for k in kinds]
     return [p for p in probs if only is None or p.name in only.split(",")]
 
 
-def time_problem(lca, p, ws, flush, steps, warmup, tensors=None):
+def time_problem(lca, p, ws, flush, steps, warmup, tensors=None, dropout=None):
     """Median forward and backward milliseconds of one problem (L2 flushed
     before every timed call pair), with its attended-cell count."""
     import torch
@@ -102,11 +106,11 @@ def time_problem(lca, p, ws, flush, steps, warmup, tensors=None):
         e = ev[s - warmup] if s >= warmup else None
         if e:
             e[0].record(stream)
-        lca.attn_fwd(q, k, v, p.segments, p.mask, p.scale, out=o, lse=lse, workspace=ws, call=call)
+        lca.attn_fwd(q, k, v, p.segments, p.mask, p.scale, out=o, lse=lse, workspace=ws, call=call, dropout=dropout)
         if e:
             e[1].record(stream)
         lca.attn_bwd(do, q, k, v, o, lse, p.segments, p.mask, p.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-                     call=call)
+                     call=call, dropout=dropout)
         if e:
             e[2].record(stream)
     torch.cuda.synchronize()
@@ -514,7 +518,7 @@ def run_workload(args, lca, dev, rank, world, barrier):
     launches0 = lca.launch_count()
     rows = {}
     for p in probs:
-        rows[p.name] = time_problem(lca, p, ws, flush, args.steps, args.warmup)
+        rows[p.name] = time_problem(lca, p, ws, flush, args.steps, args.warmup, dropout=DROPOUT.get(args.workload))
         torch.cuda.empty_cache()
     launches = lca.launch_count() - launches0
     clk = clocks.stop()
@@ -528,6 +532,7 @@ def run_workload(args, lca, dev, rank, world, barrier):
         "warmup": args.warmup, "ms_per_step": tot_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16; seeded lengths and maps)",
         "config": {"workload": WORKLOADS[args.workload], "problems": [p.name for p in probs], "head_dim": 128,
+                   "dropout_p": DROPOUT[args.workload][1] if args.workload in DROPOUT else 0.0,
                    "l2": "flushed before every timed forward+backward (256 MiB write)",
                    "timing": "per problem: median of the timed steps; a step = every problem once",
                    "parallelism": "replicas" if world > 1 else "single GPU"},

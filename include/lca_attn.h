@@ -145,6 +145,34 @@ LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, 
                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Attention dropout ("长上下文能力：FlashAttention vs. RingAttention",
+ * FlashAttention-1 核心优化, 算子融合: dropout fused with the matmuls, the
+ * mask and the softmax).  Inverted dropout on the probabilities:
+ *     O = (P * Z / kp) V,  LSE that of P (unchanged by dropout),
+ * with t = floor(256 p + 1/2) (at most 255) and kp = (256 - t) / 256.  Z_ij
+ * for query head h, query row i (global packed index) and key j (counted
+ * from the first key of row i's segment) is 1 iff byte j % 4 of word
+ * (j % 16) / 4 of Philox4x32-10(counter = (j / 16, i, h, 0), key = (seed
+ * low 32 bits, seed high 32 bits)) is >= t; the same Z is regenerated by the
+ * backward, so a forward and a backward called with equal lca_dropout values
+ * are consistent.  p must satisfy 0 <= p < 1 (LCA_ERR_INVALID_ARG
+ * otherwise); t = 0 computes exactly what lca_attn_fwd / lca_attn_bwd do. */
+typedef struct {
+  float p;       /* drop probability */
+  uint64_t seed; /* Philox key */
+} lca_dropout;
+
+/* lca_attn_fwd with dropout; dropout NULL means none. */
+LCA_API lca_status lca_attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const lca_shape* shape, const lca_mask_desc* mask, const lca_dropout* dropout,
+                                void* workspace, size_t workspace_bytes, void* stream);
+/* lca_attn_bwd with dropout: o and lse must come from lca_attn_fwd_dropout
+ * with the same shape, mask and dropout values; dropout NULL means none. */
+LCA_API lca_status lca_attn_bwd_dropout(const void* dout, const void* q, const void* k, const void* v,
+                                const void* o, const float* lse, void* dq, void* dk, void* dv,
+                                const lca_shape* shape, const lca_mask_desc* mask, const lca_dropout* dropout,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* Merge of partial forward results ("长上下文能力：FlashAttention vs.
  * RingAttention", Blockwise Parallel Transformer and RingAttention sections:
  * attention over a union of disjoint key blocks is assembled from each

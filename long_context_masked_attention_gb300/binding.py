@@ -26,7 +26,7 @@ STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "L
 EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
             "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
             "lca_last_error_detail", "lca_attn_fwd_static_workspace", "lca_status_string", "lca_version",
-            "lca_attn_merge", "lca_cad_plan")
+            "lca_attn_merge", "lca_cad_plan", "lca_attn_fwd_dropout", "lca_attn_bwd_dropout")
 PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
 
 
@@ -65,6 +65,10 @@ class Shape_t(C.Structure):
                 ("n_seg", C.c_int32), ("segs", C.POINTER(Segment_t)), ("scale", C.c_float)]
 
 
+class Dropout_t(C.Structure):
+    _fields_ = [("p", C.c_float), ("seed", C.c_uint64)]
+
+
 _lib = None
 
 
@@ -82,6 +86,10 @@ def load(path: str = LIB_PATH):
     lib.lca_attn_fwd.argtypes = [vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp, C.c_size_t, vp]
     lib.lca_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp,
                                  C.c_size_t, vp]
+    lib.lca_attn_fwd_dropout.argtypes = [vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t),
+                                         C.POINTER(Dropout_t), vp, C.c_size_t, vp]
+    lib.lca_attn_bwd_dropout.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, C.POINTER(Shape_t),
+                                         C.POINTER(MaskDesc_t), C.POINTER(Dropout_t), vp, C.c_size_t, vp]
     lib.lca_mask_materialize.argtypes = [C.POINTER(Shape_t), C.POINTER(MaskDesc_t), C.c_int32, C.c_int32, vp, vp,
                                          C.c_size_t, vp]
     lib.lca_mask_tile_classes.argtypes = lib.lca_mask_materialize.argtypes
@@ -237,8 +245,18 @@ def _workspace(call, for_bwd, workspace, device):
 
 
 # ------------------------------------------------------------------ entry points
-def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=None, stream=None, call=None):
-    """q [Tq,Hq,128], k/v [Tk,Hkv,128] bf16 CUDA tensors -> (o, lse[Hq,Tq])."""
+def _dropout(dropout):
+    """(seed, p) -> lca_dropout, or None."""
+    if dropout is None:
+        return None
+    seed, p = dropout
+    return Dropout_t(float(p), int(seed) & 0xFFFFFFFFFFFFFFFF)
+
+
+def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=None, stream=None, call=None,
+             dropout=None):
+    """q [Tq,Hq,128], k/v [Tk,Hkv,128] bf16 CUDA tensors -> (o, lse[Hq,Tq]).
+    dropout: (seed, p) for attention dropout with drop probability p."""
     import torch
 
     Tq, Hq, d = q.shape
@@ -249,9 +267,16 @@ def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=N
     if lse is None:
         lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
     workspace = _workspace(call, False, workspace, q.device)
-    _check(load().lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                               C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(), workspace.numel(),
-                               _stream(stream)), "lca_attn_fwd")
+    drop = _dropout(dropout)
+    if drop is None:
+        _check(load().lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(), workspace.numel(),
+                                   _stream(stream)), "lca_attn_fwd")
+    else:
+        _check(load().lca_attn_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                           C.byref(call.shape), C.byref(call.mask), C.byref(drop),
+                                           workspace.data_ptr(), workspace.numel(), _stream(stream)),
+               "lca_attn_fwd_dropout")
     return out, lse
 
 
@@ -320,8 +345,8 @@ def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
 
 
 def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, dv=None, workspace=None, stream=None,
-             call=None):
-    """Returns (dq, dk, dv) bf16."""
+             call=None, dropout=None):
+    """Returns (dq, dk, dv) bf16.  dropout: the (seed, p) the forward used."""
     import torch
 
     Tq, Hq, d = q.shape
@@ -331,9 +356,14 @@ def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, d
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     workspace = _workspace(call, True, workspace, q.device)
-    _check(load().lca_attn_bwd(do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), C.byref(call.shape), C.byref(call.mask),
-                               workspace.data_ptr(), workspace.numel(), _stream(stream)), "lca_attn_bwd")
+    drop = _dropout(dropout)
+    args = (do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+            dk.data_ptr(), dv.data_ptr(), C.byref(call.shape), C.byref(call.mask))
+    tail = (workspace.data_ptr(), workspace.numel(), _stream(stream))
+    if drop is None:
+        _check(load().lca_attn_bwd(*args, *tail), "lca_attn_bwd")
+    else:
+        _check(load().lca_attn_bwd_dropout(*args, C.byref(drop), *tail), "lca_attn_bwd_dropout")
     return dq, dk, dv
 
 

@@ -523,15 +523,46 @@ lca_status upload(Call& c) {
   return LCA_OK;
 }
 
-AttnArgs base_args(const Call& c) {
+// Dropout parameters: threshold t = floor(256 p + 1/2) capped at 255 (t = 0
+// turns dropout off), keep probability (256 - t) / 256.
+struct Drop {
+  int t = 0;
+  uint64_t seed = 0;
+  float keep = 1.f, inv = 1.f;
+};
+
+lca_status parse_dropout(const lca_dropout* d, Drop& out) {
+  out = Drop{};
+  if (!d) return LCA_OK;
+  const double p = d->p;
+  if (!(p >= 0.0 && p < 1.0)) return LCA_ERR_INVALID_ARG;  // also rejects NaN
+  out.t = std::min(255, static_cast<int>(std::floor(256.0 * p + 0.5)));
+  out.seed = d->seed;
+  out.keep = static_cast<float>((256 - out.t) / 256.0);
+  out.inv = static_cast<float>(256.0 / (256 - out.t));
+  return LCA_OK;
+}
+
+AttnArgs base_args(const Call& c, const Drop& dr) {
   AttnArgs a{};
   a.pv = c.V;
   a.status = reinterpret_cast<int*>(c.ws + c.L.status);
   a.wait_limit_ns = wait_limit_ns();
   a.scale = c.P.scale;
   a.scale_log2 = c.P.scale * 1.4426950408889634f;
+  a.drop_t = dr.t;
+  a.drop_inv = dr.inv;
+  a.drop_keys = philox_round_keys(dr.seed);
   return a;
 }
+
+lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const lca_shape* shape,
+                         const lca_mask_desc* mask, const lca_dropout* dropout, void* workspace,
+                         size_t workspace_bytes, void* stream);
+lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
+                         const lca_mask_desc* mask, const lca_dropout* dropout, void* workspace,
+                         size_t workspace_bytes, void* stream);
 
 }  // namespace
 }  // namespace lca
@@ -553,7 +584,7 @@ const char* lca_status_string(lca_status s) {
   return "unknown status";
 }
 
-int32_t lca_version(void) { return 100; }
+int32_t lca_version(void) { return 101; }
 
 lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases) {
   if (events && (n_events < 2 || (n_events & 1))) return LCA_ERR_INVALID_ARG;
@@ -581,8 +612,40 @@ lca_status lca_workspace_size(const lca_shape* shape, const lca_mask_desc* mask,
 
 lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_fwd_impl(q, k, v, o, lse, shape, mask, nullptr, workspace, workspace_bytes, stream);
+}
+
+lca_status lca_attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const lca_shape* shape, const lca_mask_desc* mask, const lca_dropout* dropout,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_fwd_impl(q, k, v, o, lse, shape, mask, dropout, workspace, workspace_bytes, stream);
+}
+
+lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                        const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
+                        const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_impl(dout, q, k, v, o, lse, dq, dk, dv, shape, mask, nullptr, workspace, workspace_bytes, stream);
+}
+
+lca_status lca_attn_bwd_dropout(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                                const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
+                                const lca_mask_desc* mask, const lca_dropout* dropout, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  return attn_bwd_impl(dout, q, k, v, o, lse, dq, dk, dv, shape, mask, dropout, workspace, workspace_bytes, stream);
+}
+}  // extern "C"
+
+namespace lca {
+namespace {
+
+lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, const lca_shape* shape,
+                         const lca_mask_desc* mask, const lca_dropout* dropout, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Drop dr;
+  lca_status r = parse_dropout(dropout, dr);
+  if (r != LCA_OK) return r;
   Call c;
-  lca_status r = prepare(c, shape, mask, workspace, workspace_bytes, stream, true, false);
+  r = prepare(c, shape, mask, workspace, workspace_bytes, stream, true, false);
   if (r != LCA_OK) return r;
   const HostPlan& P = c.P;
   if ((P.Tq > 0 && (!q || !o || !lse)) || (P.Tk > 0 && (!k || !v))) return LCA_ERR_INVALID_ARG;
@@ -613,7 +676,7 @@ lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
     launch_plan_fwd(c.V, tcls, wl, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
-    AttnArgs a = base_args(c);
+    AttnArgs a = base_args(c, dr);
     a.cnt = wl.cnt;
     a.order = wl.order;
     a.entries = wl.entries;
@@ -634,6 +697,11 @@ lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, fl
   LCA_CUDA(cudaGetLastError());
   return LCA_OK;
 }
+
+}  // namespace
+}  // namespace lca
+
+extern "C" {
 
 lca_status lca_attn_merge(const void* const* o_parts, const float* const* lse_parts, int32_t n_parts, void* o,
                           float* lse, int32_t Tq, int32_t Hq, int32_t d, void* stream) {
@@ -660,11 +728,20 @@ lca_status lca_attn_merge(const void* const* o_parts, const float* const* lse_pa
   return LCA_OK;
 }
 
-lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
-                        const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
-                        const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace lca {
+namespace {
+
+lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
+                         const lca_mask_desc* mask, const lca_dropout* dropout, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  Drop dr;
+  lca_status r = parse_dropout(dropout, dr);
+  if (r != LCA_OK) return r;
   Call c;
-  lca_status r = prepare(c, shape, mask, workspace, workspace_bytes, stream, true, true);
+  r = prepare(c, shape, mask, workspace, workspace_bytes, stream, true, true);
   if (r != LCA_OK) return r;
   const HostPlan& P = c.P;
   if ((P.Tq > 0 && (!dout || !q || !o || !lse || !dq)) || (P.Tk > 0 && (!k || !v || !dk || !dv)))
@@ -690,7 +767,7 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
   float* D = reinterpret_cast<float*>(c.ws + c.L.D);
   float* lse2 = reinterpret_cast<float*>(c.ws + c.L.lse2);
   int ph = phase_begin(2, c.st);
-  launch_d_prepass(o, dout, lse, D, lse2, P.Tq, P.Hq, c.st);
+  launch_d_prepass(o, dout, lse, D, lse2, P.Tq, P.Hq, dr.keep, c.st);
   phase_end(ph, c.st);
   uint32_t* hist = reinterpret_cast<uint32_t*>(c.ws + c.L.hist);
   int* counters = reinterpret_cast<int*>(c.ws + c.L.counters);
@@ -721,7 +798,7 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     launch_sort(wl, c.st);
     launch_split_dkv(wl, usteps, sp, sms, c.st);
     phase_end(ph, c.st);
-    AttnArgs a = base_args(c);
+    AttnArgs a = base_args(c, dr);
     a.cnt = wl.cnt;
     a.order = wl.order;
     a.entries = wl.entries;
@@ -759,7 +836,7 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
     launch_plan_dq(c.V, tcls, wl, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
-    AttnArgs a = base_args(c);
+    AttnArgs a = base_args(c, dr);
     a.cnt = wl.cnt;
     a.order = wl.order;
     a.entries = wl.entries;
@@ -783,6 +860,11 @@ lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const vo
   LCA_CUDA(cudaGetLastError());
   return LCA_OK;
 }
+
+}  // namespace
+}  // namespace lca
+
+extern "C" {
 
 lca_status lca_mask_materialize(const lca_shape* shape, const lca_mask_desc* mask, int32_t head, int32_t seg,
                                 uint8_t* out, void* workspace, size_t workspace_bytes, void* stream) {

@@ -18,9 +18,14 @@
 //    then dQ += dS K.
 // Both are persistent (one CTA per SM), claim cost-sorted items through an
 // atomic counter, and use one TMA producer warp and one MMA-issue warp.
+// Dropout (a compile-time instantiation of both) regenerates the forward's
+// keep bits Z from the same counters: with P~ = P * Z / kp and D scaled by kp
+// in the prepass, the kernels form dS' = P * (Z * dP~ - kp D) = kp dS and
+// P * Z, and the epilogues multiply dQ, dK, dV by 1 / kp.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "lca_dropout.cuh"
 #include "lca_internal.h"
 #include "sm103.cuh"
 
@@ -225,10 +230,12 @@ abort:
   mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
 }
 
-template <bool kCols>
+template <bool kCols, bool kDrop>
 __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  const DropCtx dc = make_drop_ctx(a.drop_t);
+  const float out_scale = kDrop ? a.scale * a.drop_inv : a.scale;
   const int warp = threadIdx.x >> 5;
   const int wq = warp & 3, half = warp >> 2;
   const int lane = threadIdx.x & 31;
@@ -256,6 +263,13 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
       const uint32_t cls = (e >> 24) & 3u;
       const int kt = static_cast<int>(e & 0xFFFFFFu);
+      uint32_t kb[2] = {~0u, ~0u};  // dropout keep bits of this thread's 64 keys, drawn while S is computed
+      if (kDrop) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          kb[c] = keep32(dc, a.drop_keys, static_cast<uint32_t>(sg.q_off + i), static_cast<uint32_t>(inf.head),
+                         static_cast<uint32_t>(kt * 8 + half * 4 + 2 * c));
+      }
       if (!waitw(&bar[B_SFULL], sdp & 1, a, 131)) return;
       tc_fence_after();
       float s[64], dp[64];
@@ -287,7 +301,13 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       for (int k = 0; k < 32; ++k) {
         const float p0 = ex2_approx(fmaf(s[2 * k], sl2, -lse2));
         const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, -lse2));
-        pk[k] = pack_bf16x2(p0 * (dp[2 * k] - Dv), p1 * (dp[2 * k + 1] - Dv));
+        if (kDrop) {  // dS' = P (Z dP~ - kp D)
+          const float z0 = ((kb[k >> 4] >> ((2 * k) & 31)) & 1u) ? dp[2 * k] : 0.f;
+          const float z1 = ((kb[k >> 4] >> ((2 * k + 1) & 31)) & 1u) ? dp[2 * k + 1] : 0.f;
+          pk[k] = pack_bf16x2(p0 * (z0 - Dv), p1 * (z1 - Dv));
+        } else {
+          pk[k] = pack_bf16x2(p0 * (dp[2 * k] - Dv), p1 * (dp[2 * k + 1] - Dv));
+        }
       }
       // dS (bf16) into TMEM buffer db, this thread's 64 key columns = 32 packed columns
       const int db = tiles & 1;
@@ -315,7 +335,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
 #pragma unroll
           for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(qrow + 32 * c + 8 * u) = pack8(f + 8 * u, a.scale);
+          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(qrow + 32 * c + 8 * u) = pack8(f + 8 * u, out_scale);
         }
       }
     } else if (valid) {
@@ -326,7 +346,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   }
 }
 
-template <bool kCols>
+template <bool kCols, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
@@ -358,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
-    compute<kCols>(a, sm, bar, items, tbase);
+    compute<kCols, kDrop>(a, sm, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -397,11 +417,15 @@ struct Item {
   int slot;   // partial-sum slot of a chunk, -1 when the item writes dK/dV itself
 };
 
-// Per-step data the producer warp stages for the compute warps (buffer b of
-// two): the 64 query rows' LSE (base 2) and D, the mask words of a partial
-// tile, and the step's class.  The compute warps read only shared memory.
+// Per-step data the producer warp stages for the compute warps (ring slot b):
+// the 64 query rows' LSE (base 2) and D, the mask words of a partial tile,
+// the step's class, first global row and query head.  The compute warps read
+// only shared memory.
 struct StepMeta {
-  int cls, pad0, pad1, pad2;
+  int cls;
+  int row0;  // global query row of the step's first row (dropout counters)
+  int head;  // query head of the step
+  int pad;
 };
 __device__ __forceinline__ float* stat_lse2(uint8_t* sm, int b) {
   return reinterpret_cast<float*>(sm + kOffStat + b * kStatBytes);
@@ -545,7 +569,12 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                   sw[wd] = mask_bits<kCols>(pv.mask, sg, hm, r0 + (wd >> 2), inf.kt * kTile + 32 * (wd & 3));
                 }
               }
-              if (lane == 0) stat_meta(sm, b)->cls = static_cast<int>(cls);
+              if (lane == 0) {
+                StepMeta* meta = stat_meta(sm, b);
+                meta->cls = static_cast<int>(cls);
+                meta->row0 = sg.q_off + r0;
+                meta->head = h;
+              }
               __syncwarp();
               if (lane == 0) mbar_arrive(&bar[B_MFULL + b]);
               if (reuse >= 1 && !waitw(&bar[B_QEMPTY + b], (reuse - 1) & 1, a, 212)) goto abort;
@@ -654,8 +683,11 @@ abort:
   mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
 }
 
+template <bool kDrop>
 __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
+  const DropCtx dc = make_drop_ctx(a.drop_t);
+  const float dv_scale = kDrop ? a.drop_inv : 1.f, dk_scale = kDrop ? a.scale * a.drop_inv : a.scale;
   const int warp = threadIdx.x >> 5;
   const int wq = warp & 3, half = warp >> 2;  // half: which 32 of the 64 query columns
   const int lane = threadIdx.x & 31;
@@ -679,7 +711,16 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       const float* s_lse2 = stat_lse2(sm, r);
       const float* s_D = stat_D(sm, r);
       const uint32_t* s_mask = stat_mask(sm, r);
-      const int cls = stat_meta(sm, r)->cls;
+      const StepMeta meta = *stat_meta(sm, r);
+      const int cls = meta.cls;
+      uint32_t kb = ~0u;  // dropout keep bits: bit k = query 32*half + k for this thread's key
+      if (kDrop) {
+        // lane l draws query row 32*half + l over the warp's 32 keys, then the
+        // warp transposes the 32 x 32 bits so that each lane holds its key's
+        const uint32_t rowbits = keep32(dc, a.drop_keys, static_cast<uint32_t>(meta.row0 + 32 * half + lane),
+                                        static_cast<uint32_t>(meta.head), static_cast<uint32_t>(inf.kt * 8 + wq * 2));
+        kb = warp_transpose_bits(rowbits, lane);
+      }
       if (!waitw(&bar[B_SFULL + b], (steps >> 1) & 1, a, 231)) return;
       tc_fence_after();
       float sv[32], dp[32];
@@ -706,8 +747,14 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         const int q0 = 32 * half + 2 * k;
         const float p0 = ex2_approx(fmaf(sv[2 * k], sl2, -s_lse2[q0]));
         const float p1 = ex2_approx(fmaf(sv[2 * k + 1], sl2, -s_lse2[q0 + 1]));
-        pp[k] = pack_bf16x2(p0, p1);
-        pd[k] = pack_bf16x2(p0 * (dp[2 * k] - s_D[q0]), p1 * (dp[2 * k + 1] - s_D[q0 + 1]));
+        if (kDrop) {  // P~ = P Z for dV; dS' = P Z dP~ - P kp D for dK
+          const float pz0 = ((kb >> (2 * k)) & 1u) ? p0 : 0.f, pz1 = ((kb >> (2 * k + 1)) & 1u) ? p1 : 0.f;
+          pp[k] = pack_bf16x2(pz0, pz1);
+          pd[k] = pack_bf16x2(fmaf(pz0, dp[2 * k], -p0 * s_D[q0]), fmaf(pz1, dp[2 * k + 1], -p1 * s_D[q0 + 1]));
+        } else {
+          pp[k] = pack_bf16x2(p0, p1);
+          pd[k] = pack_bf16x2(p0 * (dp[2 * k] - s_D[q0]), p1 * (dp[2 * k + 1] - s_D[q0 + 1]));
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_MEMPTY + r]);  // done with this step's staged data
@@ -758,7 +805,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
 #pragma unroll
           for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dV + orow + 32 * c + 8 * u) = pack8(f + 8 * u, 1.f);
+          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dV + orow + 32 * c + 8 * u) = pack8(f + 8 * u, dv_scale);
         }
         tmem_ld32(tbase + tl + 384 + half * 64 + 32 * c, r);
         tmem_ld_wait();
@@ -767,7 +814,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
           for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(dK + orow + 32 * c + 8 * u) = pack8(f + 8 * u, a.scale);
+            *reinterpret_cast<uint4*>(dK + orow + 32 * c + 8 * u) = pack8(f + 8 * u, dk_scale);
         }
       }
     } else if (valid) {
@@ -781,7 +828,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   }
 }
 
-template <bool kCols>
+template <bool kCols, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
@@ -815,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
-    compute(a, sm, bar, items, tbase);
+    compute<kDrop>(a, sm, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -853,9 +900,11 @@ __global__ void __launch_bounds__(256) reduce_kernel(const AttnArgs a) {
       sk.x += k.x; sk.y += k.y; sk.z += k.z; sk.w += k.w;
     }
     const size_t row = (static_cast<size_t>(grp.k_off + jg) * pv.Hkv + g) * kHeadDim + d4;
-    *reinterpret_cast<uint2*>(dV + row) = make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w));
+    const float vs = a.drop_inv, ks = a.scale * a.drop_inv;  // drop_inv = 1 without dropout
+    *reinterpret_cast<uint2*>(dV + row) =
+        make_uint2(pack_bf16x2(sv.x * vs, sv.y * vs), pack_bf16x2(sv.z * vs, sv.w * vs));
     *reinterpret_cast<uint2*>(dK + row) =
-        make_uint2(pack_bf16x2(sk.x * a.scale, sk.y * a.scale), pack_bf16x2(sk.z * a.scale, sk.w * a.scale));
+        make_uint2(pack_bf16x2(sk.x * ks, sk.y * ks), pack_bf16x2(sk.z * ks, sk.w * ks));
   }
 }
 
@@ -866,33 +915,47 @@ void launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const AttnArgs& a, int num_sms, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(dq::dq_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
-    cudaFuncSetAttribute(dq::dq_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
     configured = true;
   }
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
-  if (a.pv.mask.kind == kFlashMask)
-    dq::dq_kernel<true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  const bool cols = a.pv.mask.kind == kFlashMask, drop = a.drop_t > 0;
+  if (cols && drop)
+    dq::dq_kernel<true, true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (cols)
+    dq::dq_kernel<true, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (drop)
+    dq::dq_kernel<false, true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
   else
-    dq::dq_kernel<false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dq::dq_kernel<false, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
 }
 
 void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                     const AttnArgs& a, int num_sms, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(dkv::dkv_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
-    cudaFuncSetAttribute(dkv::dkv_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
     configured = true;
   }
   // the item count is known on the device only (split pass); surplus CTAs find no work and exit
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
-  if (a.pv.mask.kind == kFlashMask)
-    dkv::dkv_kernel<true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  const bool cols = a.pv.mask.kind == kFlashMask, drop = a.drop_t > 0;
+  if (cols && drop)
+    dkv::dkv_kernel<true, true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (cols)
+    dkv::dkv_kernel<true, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (drop)
+    dkv::dkv_kernel<false, true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
   else
-    dkv::dkv_kernel<false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dkv::dkv_kernel<false, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
 }
 
 void launch_dkv_reduce(const AttnArgs& a, cudaStream_t st) {

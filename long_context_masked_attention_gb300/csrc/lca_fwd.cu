@@ -25,6 +25,11 @@
 //                TMEM only when its running max grows by more than 2^8,
 //                writes P back into TMEM, and at the end normalises O and
 //                writes O and LSE.
+// With dropout (a compile-time instantiation), each softmax thread draws the
+// keep bytes of its row chunk by chunk (two Philox calls per 32 keys); P goes
+// into TMEM with the dropped entries zeroed (a byte-permute mask over the
+// packed bf16 pairs) while the row sum l keeps them, and the final
+// normalisation multiplies by 1/kp.
 // Per sub-tile the MMA thread issues O_x += P_x(t-1) V(t-1) and then
 // S_x(t) = Q_x K(t)^T (tcgen05.mma executes in issue order, so S_x(t) does not
 // overwrite P_x(t-1) before it is read); while one warpgroup computes
@@ -32,6 +37,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "lca_dropout.cuh"
 #include "lca_internal.h"
 #include "sm103.cuh"
 
@@ -280,9 +286,13 @@ __device__ __forceinline__ float tile_row_max(uint32_t tS, const uint32_t (&mb)[
 // P = 2^(s*scale*log2(e) - base) for the thread's row, written as bf16 pairs
 // over the first 64 columns of S in TMEM (chunk c's 16 pair-columns land on
 // columns 16c..16c+15, which belong to chunks already read); returns the row
-// sum of P in f32.
-template <bool kMasked>
-__device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], float sl2, float base) {
+// sum of P in f32.  With dropout, chunk c draws the keep bytes of its 32 keys
+// (key groups g0 + 2c, g0 + 2c + 1 of query row `row`); dropped entries are
+// written as 0 but still counted in the sum.
+template <bool kMasked, bool kDrop>
+__device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], float sl2, float base,
+                                          const AttnArgs& a, const DropCtx& dc, uint32_t row, uint32_t head,
+                                          uint32_t g0) {
   const uint64_t sl2x2 = f2(sl2, sl2), nb2 = f2(-base, -base);
   uint64_t acc[4] = {0, 0, 0, 0};  // four independent packed partial sums
   uint32_t ra[32], rb[32];
@@ -294,6 +304,19 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], 
     uint32_t(&nxt)[32] = (c & 1) ? ra : rb;
     if (c + 1 < 4) tmem_ld32(tS + 32 * (c + 1), nxt);
     uint32_t pk[16];
+    uint32_t ks[8];  // keep signs of the chunk's 32 keys, 4 per word
+    if (kDrop) {
+      const uint4 r0 = philox4x32_10(g0 + 2 * c, row, head, 0u, a.drop_keys);
+      const uint4 r1 = philox4x32_10(g0 + 2 * c + 1, row, head, 0u, a.drop_keys);
+      ks[0] = keep_signs(r0.x, dc);
+      ks[1] = keep_signs(r0.y, dc);
+      ks[2] = keep_signs(r0.z, dc);
+      ks[3] = keep_signs(r0.w, dc);
+      ks[4] = keep_signs(r1.x, dc);
+      ks[5] = keep_signs(r1.y, dc);
+      ks[6] = keep_signs(r1.z, dc);
+      ks[7] = keep_signs(r1.w, dc);
+    }
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
       const uint64_t sv = f2(score<kMasked>(cur[2 * k], mb[c], 2 * k), score<kMasked>(cur[2 * k + 1], mb[c], 2 * k + 1));
@@ -301,6 +324,7 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], 
       const uint64_t pp = f2(ex2_approx(f2lo(xx)), ex2_approx(f2hi(xx)));
       acc[k & 3] = fadd2(acc[k & 3], pp);
       pk[k] = pack_bf16x2(f2lo(pp), f2hi(pp));
+      if (kDrop) pk[k] &= (k & 1) ? keep_halves<1>(ks[k >> 1]) : keep_halves<0>(ks[k >> 1]);
     }
     tmem_st16(tS + 16 * c, pk);
   }
@@ -308,7 +332,7 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], 
   return f2lo(t) + f2hi(t);
 }
 
-template <bool kCols>
+template <bool kCols, bool kDrop>
 __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
@@ -320,6 +344,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
   const uint32_t tO = tbase + tl + 256 + 128 * x;
   __nv_bfloat16* O = static_cast<__nv_bfloat16*>(a.o);
   const float sl2 = a.scale_log2;
+  const DropCtx dc = make_drop_ctx(a.drop_t);
   uint32_t s_cons = 0, p_prod = 0;
   for (int it = 0;; ++it) {
     const int slot = it & 1;
@@ -363,7 +388,10 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       // P = exp2(s*scale*log2e - m) as bf16 pairs, written over the first 64
       // columns of S_x in TMEM (the A operand of O_x += P_x V)
       const float base = (m_use == -INFINITY) ? 0.f : m_use;
-      const float sum = (cls == kTilePartial) ? tile_exp<true>(tS, mb, sl2, base) : tile_exp<false>(tS, mb, sl2, base);
+      const uint32_t grow = static_cast<uint32_t>(sg.q_off + i), g0 = static_cast<uint32_t>(kt * 8);
+      const float sum = (cls == kTilePartial)
+                            ? tile_exp<true, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0)
+                            : tile_exp<false, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0);
       l = l * factor + sum;
       if (__any_sync(0xFFFFFFFFu, need)) {
         // the previous O_x += P_x V must have finished before O_x is rescaled
@@ -391,7 +419,8 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
     if (any) {
       if (!waitw(&bar[B_OFULL + x], (p_prod - 1) & 1, a, 36 + x)) return;
       tc_fence_after();
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      float inv = (l > 0.f) ? 1.f / l : 0.f;
+      if (kDrop) inv *= a.drop_inv;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
@@ -421,7 +450,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
   }
 }
 
-template <bool kCols>
+template <bool kCols, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
@@ -462,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sQ, sKV, bar, items, tbase);
   } else {
-    softmax_wg<kCols>(a, warp >> 2, bar, items, tbase);
+    softmax_wg<kCols, kDrop>(a, warp >> 2, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -478,16 +507,23 @@ void launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap&
                 cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    cudaFuncSetAttribute(fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     configured = true;
   }
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
-  if (a.pv.mask.kind == kFlashMask)
-    fwd_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  const bool cols = a.pv.mask.kind == kFlashMask, drop = a.drop_t > 0;
+  if (cols && drop)
+    fwd_kernel<true, true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  else if (cols)
+    fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  else if (drop)
+    fwd_kernel<false, true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
   else
-    fwd_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+    fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
 }
 
 }  // namespace lca

@@ -6,6 +6,7 @@
 #include <cstdint>
 
 #include "lca_common.cuh"
+#include "lca_dropout.cuh"
 
 namespace lca {
 
@@ -76,8 +77,9 @@ struct MergeArgs {
   int Tq, Hq;
 };
 void launch_merge(const MergeArgs& m, cudaStream_t st);
+// D = dmul * rowsum(dO * O): dmul is the keep probability under dropout, 1 otherwise.
 void launch_d_prepass(const void* o, const void* dout, const float* lse, float* D, float* lse2, int Tq, int Hq,
-                      cudaStream_t st);
+                      float dmul, cudaStream_t st);
 void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream_t st);
 void launch_probe_timeout(int* status, unsigned long long limit_ns, cudaStream_t st);
 
@@ -105,6 +107,11 @@ struct AttnArgs {
   unsigned long long wait_limit_ns;
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
+  // dropout on P: threshold t (0 = off; keep probability (256 - t) / 256),
+  // the Philox round keys, and 1 / keep probability (1 without dropout)
+  int drop_t;
+  float drop_inv;
+  PhiloxKeys drop_keys;
   // tensors
   void* o;
   float* lse;

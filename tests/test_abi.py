@@ -133,3 +133,30 @@ def test_workspace_too_small_is_rejected(L):
                           n.value - 1, None) == 3
     assert L.lca_attn_fwd(fake, fake, fake, fake, fake, C.byref(call.shape), C.byref(call.mask), C.c_void_p(0x10001),
                           n.value, None) == 3  # misaligned
+
+
+@pytest.mark.parametrize("p", [-0.1, 1.0, 1.5, float("nan"), float("inf")])
+def test_dropout_probability_out_of_range_rejected(L, p):
+    call = B.marshal(256, 256, 4, 2, 128, [Segment(0, 256, 0, 256)], MaskSpec("CAUSAL"))
+    fake = C.c_void_p(0x1000)
+    drop = B.Dropout_t(p, 7)
+    assert L.lca_attn_fwd_dropout(fake, fake, fake, fake, fake, C.byref(call.shape), C.byref(call.mask),
+                                  C.byref(drop), C.c_void_p(0x10000), 1 << 30, None) == 1
+    assert L.lca_attn_bwd_dropout(fake, fake, fake, fake, fake, fake, fake, fake, fake, C.byref(call.shape),
+                                  C.byref(call.mask), C.byref(drop), C.c_void_p(0x10000), 1 << 30, None) == 1
+
+
+def test_dropout_entry_points_validate_like_the_plain_ones(L):
+    """A valid probability passes on to the same shape and workspace checks."""
+    call = B.marshal(256, 256, 4, 2, 128, [Segment(0, 256, 0, 256)], MaskSpec("CAUSAL"))
+    n = C.c_size_t(0)
+    assert L.lca_workspace_size(C.byref(call.shape), C.byref(call.mask), 1, C.byref(n)) == 0
+    fake = C.c_void_p(0x1000)
+    drop = B.Dropout_t(0.1, 7)
+    assert L.lca_attn_fwd_dropout(fake, fake, fake, fake, fake, C.byref(call.shape), C.byref(call.mask),
+                                  C.byref(drop), C.c_void_p(0x10000), 16, None) == 3
+    assert L.lca_attn_bwd_dropout(fake, fake, fake, fake, fake, fake, fake, fake, fake, C.byref(call.shape),
+                                  C.byref(call.mask), C.byref(drop), C.c_void_p(0x10000), n.value - 1, None) == 3
+    bad = B.marshal(256, 256, 6, 4, 128, [Segment(0, 256, 0, 256)], MaskSpec("CAUSAL"))  # Hq % Hkv != 0
+    assert L.lca_attn_fwd_dropout(fake, fake, fake, fake, fake, C.byref(bad.shape), C.byref(bad.mask),
+                                  C.byref(drop), C.c_void_p(0x10000), 1 << 30, None) == 1
