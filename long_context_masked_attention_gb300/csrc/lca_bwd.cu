@@ -11,8 +11,8 @@
 //    K and V resident, walks every query head of the group and every 64-row
 //    query step that attends the tile (key-major list), and accumulates dV
 //    and dK in TMEM.  Per step: S^T = K Q^T and dP^T = V dO^T (TMEM),
-//    P^T, dS^T computed by 8 warps (thread = key row) and staged in shared
-//    memory, then dV += P^T dO and dK += dS^T Q.
+//    P^T, dS^T computed by 8 warps (thread = key row) and written back to
+//    TMEM as bf16, then dV += P^T dO and dK += dS^T Q.
 //  * dq_kernel — one work item per (query head, 128-row query tile): per key
 //    tile S = Q K^T, dP = dO V^T (TMEM), dS by 8 warps (thread = query row),
 //    then dQ += dS K.
@@ -398,8 +398,8 @@ constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTile128;
 constexpr int kOffQ = kOffV + kTile128;          // ring of 64-row Q tiles
 constexpr int kOffDO = kOffQ + kRing * kTile64;  // ring of 64-row dO tiles
-constexpr int kOffStat = kOffDO + kRing * kTile64;  // kRing buffers of: lse2[64], D[64], mask words[64][4], meta
-constexpr int kStatBytes = 64 * 4 * 2 + 64 * 4 * 4 + 16;
+constexpr int kOffStat = kOffDO + kRing * kTile64;  // kRing buffers of: lse2[64], D[64], meta
+constexpr int kStatBytes = 64 * 4 * 2 + 64;
 constexpr int kOffCtl = kOffStat + kRing * kStatBytes;
 constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
 
@@ -418,24 +418,24 @@ struct Item {
 };
 
 // Per-step data the producer warp stages for the compute warps (ring slot b):
-// the 64 query rows' LSE (base 2) and D, the mask words of a partial tile,
-// the step's class, first global row and query head.  The compute warps read
-// only shared memory.
-struct StepMeta {
+// the 64 query rows' LSE (base 2) and D, and the step's class, first rows,
+// query head, map head and segment.  The compute warps read only shared
+// memory; on a partial tile they evaluate the mask themselves.
+struct StepMeta {  // 64 bytes
   int cls;
-  int row0;  // global query row of the step's first row (dropout counters)
-  int head;  // query head of the step
-  int pad;
+  int row0;  // global query row of the step's first row
+  int r0;    // the same row, relative to the segment
+  int head;  // query head
+  int hm;    // mask map head
+  int pad0, pad1, pad2;
+  SegInfo sg;
 };
 __device__ __forceinline__ float* stat_lse2(uint8_t* sm, int b) {
   return reinterpret_cast<float*>(sm + kOffStat + b * kStatBytes);
 }
 __device__ __forceinline__ float* stat_D(uint8_t* sm, int b) { return stat_lse2(sm, b) + 64; }
-__device__ __forceinline__ uint32_t* stat_mask(uint8_t* sm, int b) {
-  return reinterpret_cast<uint32_t*>(stat_lse2(sm, b) + 128);
-}
 __device__ __forceinline__ StepMeta* stat_meta(uint8_t* sm, int b) {
-  return reinterpret_cast<StepMeta*>(stat_mask(sm, b) + 256);
+  return reinterpret_cast<StepMeta*>(stat_lse2(sm, b) + 128);
 }
 
 // The whole producer warp runs this loop; lane 0 issues the TMA copies and
@@ -561,19 +561,14 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                 cp_async_4(sd + qi, a.D + src, nb);
               }
               cp_async_mbar_arrive_noinc(&bar[B_MFULL + b]);
-              if (cls == kTilePartial) {
-                uint32_t* sw = stat_mask(sm, b);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                  const int wd = lane * 8 + u;  // word = query row * 4 + key chunk
-                  sw[wd] = mask_bits<kCols>(pv.mask, sg, hm, r0 + (wd >> 2), inf.kt * kTile + 32 * (wd & 3));
-                }
-              }
               if (lane == 0) {
                 StepMeta* meta = stat_meta(sm, b);
                 meta->cls = static_cast<int>(cls);
                 meta->row0 = sg.q_off + r0;
+                meta->r0 = r0;
                 meta->head = h;
+                meta->hm = hm;
+                meta->sg = sg;
               }
               __syncwarp();
               if (lane == 0) mbar_arrive(&bar[B_MFULL + b]);
@@ -683,7 +678,7 @@ abort:
   mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
 }
 
-template <bool kDrop>
+template <bool kCols, bool kDrop>
 __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
   const PlanView& pv = a.pv;
   const DropCtx dc = make_drop_ctx(a.drop_t);
@@ -710,15 +705,29 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       if (!waitw(&bar[B_MFULL + r], (steps / kRing) & 1, a, 234)) return;
       const float* s_lse2 = stat_lse2(sm, r);
       const float* s_D = stat_D(sm, r);
-      const uint32_t* s_mask = stat_mask(sm, r);
-      const StepMeta meta = *stat_meta(sm, r);
-      const int cls = meta.cls;
+      const StepMeta* meta_s = stat_meta(sm, r);
+      const int cls = meta_s->cls;
+      // mask bits of a partial tile, bit k = query 32*half + k for this
+      // thread's key: FlashMask reads them off the key's column bounds; the
+      // other families evaluate one query row per lane over the warp's 32
+      // keys and transpose the 32 x 32 bits across the warp
+      uint32_t mb = ~0u;
+      if (cls == kTilePartial) {
+        const SegInfo sg = meta_s->sg;
+        const int i0 = meta_s->r0 + 32 * half;
+        if constexpr (kCols) {
+          mb = flashmask_key_bits(pv.mask, sg, inf.kt * kTile + j, i0);
+        } else {
+          mb = warp_transpose_bits(mask_bits<false>(pv.mask, sg, meta_s->hm, i0 + lane, inf.kt * kTile + wq * 32),
+                                   lane);
+        }
+      }
       uint32_t kb = ~0u;  // dropout keep bits: bit k = query 32*half + k for this thread's key
       if (kDrop) {
         // lane l draws query row 32*half + l over the warp's 32 keys, then the
         // warp transposes the 32 x 32 bits so that each lane holds its key's
-        const uint32_t rowbits = keep32(dc, a.drop_keys, static_cast<uint32_t>(meta.row0 + 32 * half + lane),
-                                        static_cast<uint32_t>(meta.head), static_cast<uint32_t>(inf.kt * 8 + wq * 2));
+        const uint32_t rowbits = keep32(dc, a.drop_keys, static_cast<uint32_t>(meta_s->row0 + 32 * half + lane),
+                                        static_cast<uint32_t>(meta_s->head), static_cast<uint32_t>(inf.kt * 8 + wq * 2));
         kb = warp_transpose_bits(rowbits, lane);
       }
       if (!waitw(&bar[B_SFULL + b], (steps >> 1) & 1, a, 231)) return;
@@ -736,10 +745,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       tmem_ld_wait();
       if (cls == kTilePartial) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const uint32_t w = s_mask[(32 * half + k) * 4 + wq];
-          sv[k] = ((w >> lane) & 1u) ? sv[k] : -INFINITY;
-        }
+        for (int k = 0; k < 32; ++k) sv[k] = ((mb >> k) & 1u) ? sv[k] : -INFINITY;
       }
       uint32_t pp[16], pd[16];
 #pragma unroll
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
-    compute<kDrop>(a, sm, bar, items, tbase);
+    compute<kCols, kDrop>(a, sm, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();

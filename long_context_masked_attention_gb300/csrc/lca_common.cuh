@@ -252,6 +252,14 @@ __device__ __forceinline__ uint32_t flashmask_chunk_bits(const MaskCtx& m, const
   return bits;
 }
 
+// FlashMask, key-major: bit t = row i0 + t of the segment attends key j
+// (segment-relative), from that key's column bounds alone.
+__device__ __forceinline__ uint32_t flashmask_key_bits(const MaskCtx& m, const SegInfo& sg, int j, int i0) {
+  if (j < 0 || j >= sg.k_len) return 0u;
+  const int4 b = __ldg(m.cols + sg.k_off + j);
+  return range_bits(0, sg.q_len, i0) & ~(range_bits(b.x, b.y, i0) | range_bits(b.z, b.w, i0));
+}
+
 // Rows of [r0, r1) that column bounds b mask.
 __device__ __forceinline__ int col_masked_rows(const int4& b, int r0, int r1) {
   const int n0 = max(0, min(b.y, r1) - max(b.x, r0));
