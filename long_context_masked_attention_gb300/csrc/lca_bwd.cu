@@ -292,8 +292,10 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const uint32_t bits = mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
+          if (!__all_sync(0xFFFFFFFFu, bits == ~0u)) {  // the warp's 32 rows do not all keep the chunk
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
+            for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
+          }
         }
       }
       uint32_t pk[32];
@@ -743,7 +745,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
       }
       tmem_ld_wait();
-      if (cls == kTilePartial) {
+      if (cls == kTilePartial && !__all_sync(0xFFFFFFFFu, mb == ~0u)) {
 #pragma unroll
         for (int k = 0; k < 32; ++k) sv[k] = ((mb >> k) & 1u) ? sv[k] : -INFINITY;
       }
