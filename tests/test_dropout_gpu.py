@@ -7,7 +7,7 @@ with one-hot V the forward's O exposes Z row by row; with one-hot dO the dK/dV
 kernel's dV exposes Z key by key (through its transposed bit layout); with
 one-hot K, constant V and dO, the sign of dQ exposes Z.  Then forward and
 backward values are checked against the fp64 oracle with the same dropout on
-every static mask family, on split dK/dV units, and at the 8K sweep's full
+every static mask family and the block-sparse maps, on split dK/dV units, and at the 8K sweep's full
 size on sampled rows and the last key tile."""
 from __future__ import annotations
 
@@ -133,7 +133,7 @@ def _parity(lca, prob, drop):
     check_bwd((dq, dk, dv), oracle.attention_backward(prob, qc, kc, vc, doc, dropout=drop), what=prob.name)
 
 
-SMALL = cases.gpu_small_all()[:12] + [p for p in cases.edge_cases() if p.name in ("edge_q_gt_k", "edge_gaps")]
+SMALL = cases.gpu_small_all() + [p for p in cases.edge_cases() if p.name in ("edge_q_gt_k", "edge_gaps")]
 
 
 @pytest.mark.parametrize("prob", SMALL, ids=[p.name for p in SMALL])
