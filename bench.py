@@ -58,6 +58,17 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def tensor_peak(pk, pk_src, clk):
+    """The bf16 peak that matches the clocks sampled during the timed region:
+    the burst figure when the SM clock stayed at its maximum with no power
+    cap, else the sustained (power-capped) one."""
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    held = bool(clk.get("samples")) and sm and mx and sm >= 0.95 * mx and "sw_power_cap" not in clk.get("reasons", [])
+    if held:
+        return pk["bf16_tflops"], f"{pk_src} bf16 burst (SM clock held at its maximum, no power cap seen)"
+    return pk["bf16_tflops_sustained"], f"{pk_src} bf16 sustained (power cap seen or clock below maximum)"
+
+
 WORKLOADS = {
     "sweep8k": "static_mask_sweep_8k_gqa64x8_d128",
     "dense48k": "dense_length_sweep_1k_48k_48k_tokens_mha64_gqa64x8_d128",
@@ -468,6 +479,7 @@ def run_ours(args):
                          "first input copy to the last output copy"}
 
     pk, pk_src = peaks()
+    peak, peak_src = tensor_peak(pk, pk_src, clk)
     # dominant kernel and its roofline (algorithmic FLOPs per launch / launch time)
     alg = {"fwd": 4.0, "dkv": 8.0, "dq": 6.0}  # executed matmul FLOPs per attended cell / d
     kern = {ph: sum(v) for ph, v in phases.items() if ph in alg}
@@ -477,10 +489,11 @@ def run_ours(args):
         n_launch = len(phases[dom])
         flops_dom = alg[dom] * d * sum(nnz) * args.steps
         achieved = flops_dom / (sum(phases[dom]) * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
-                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
                     "traffic": measured_traffic(dom), "traffic_unit": "bytes per launch (ncu, cold L2)",
-                    "launches": n_launch, "peak_source": f"{pk_src} sustained bf16"}
+                    "launches": n_launch, "peak_source": peak_src,
+                    "frac_of_sustained": achieved / pk["bf16_tflops_sustained"]}
     phase_ms = {ph: sum(v) / args.steps for ph, v in phases.items()}
     per_mask = {}
     for p in probs:
@@ -492,8 +505,7 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "seq_len": 8192, "batch": 1, "heads": "64:8", "head_dim": 128,
                    "masks": [p.mask.kind for p in probs], "l2": "flushed between steps (256 MiB write)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "pct_of_peak": 100.0 * value / pk["bf16_tflops_sustained"],
-        "peak_tflops": pk["bf16_tflops_sustained"], "peak_source": f"{pk_src} bf16 sustained",
+        "pct_of_peak": 100.0 * value / peak, "peak_tflops": peak, "peak_source": peak_src,
         "roofline": roofline, "phase_ms_per_step": phase_ms, "gpu_launches": launches,
         "clocks": clk, "e2e": e2e, "per_mask": per_mask,
     }
@@ -535,6 +547,7 @@ def run_workload(args, lca, dev, rank, world, barrier):
     ms = sum(r["fwd_ms"] + r["bwd_ms"] for r in rows.values())
     tot_ms, tot_flops = aggregate(ms, flops, world, dev)
     pk, pk_src = peaks()
+    peak, peak_src = tensor_peak(pk, pk_src, clk)
     value = tot_flops / (tot_ms * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -545,8 +558,8 @@ def run_workload(args, lca, dev, rank, world, barrier):
                    "l2": "flushed before every timed forward+backward (256 MiB write)",
                    "timing": "per problem: median of the timed steps; a step = every problem once",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "pct_of_peak": 100.0 * value / pk["bf16_tflops_sustained"], "peak_tflops": pk["bf16_tflops_sustained"],
-        "peak_source": f"{pk_src} bf16 sustained", "gpu_launches": launches * world, "clocks": clk, "e2e": None,
+        "pct_of_peak": 100.0 * value / peak, "peak_tflops": peak,
+        "peak_source": peak_src, "gpu_launches": launches * world, "clocks": clk, "e2e": None,
         "per_problem": rows,
     }
     if rank == 0:
