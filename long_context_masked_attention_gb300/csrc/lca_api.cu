@@ -814,8 +814,8 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.n_work_dev = sp.n_work;
     a.partials = reinterpret_cast<float*>(c.ws + c.L.k_part);
     a.n_units = static_cast<int>(k_units);
-    a.D = D;
-    a.lse2 = lse2;
+    a.nD = D;
+    a.nlse2 = lse2;
     a.dk = dk;
     a.dv = dv;
     ph = phase_begin(4, c.st);
@@ -843,8 +843,8 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(q_rows * wl.expand);
-    a.D = D;
-    a.lse2 = lse2;
+    a.nD = D;
+    a.nlse2 = lse2;
     a.dq = dq;
     ph = phase_begin(6, c.st);
     launch_bwd_dq(tq, tk, tv, tdo, a, sms, c.st);

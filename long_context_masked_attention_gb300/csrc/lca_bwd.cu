@@ -236,12 +236,12 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
   const DropCtx dc = make_drop_ctx(a.drop_t);
   const float out_scale = kDrop ? a.scale * a.drop_inv : a.scale;
+  const uint64_t sl2x2 = f2(a.scale_log2, a.scale_log2);
   const int warp = threadIdx.x >> 5;
   const int wq = warp & 3, half = warp >> 2;
   const int lane = threadIdx.x & 31;
   const int row = wq * 32 + lane;
   const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
-  const float sl2 = a.scale_log2;
   __nv_bfloat16* dQ = static_cast<__nv_bfloat16*>(a.dq);
   uint32_t tiles = 0, sdp = 0, items_done = 0;
   for (int it = 0;; ++it) {
@@ -255,8 +255,9 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     const int i = inf.qt * kTile + row;
     const bool valid = i < sg.q_len;
     const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
-    const float lse2 = valid ? a.lse2[stat] : INFINITY;
-    const float Dv = valid ? a.D[stat] : 0.f;
+    const uint64_t nl2 = f2(valid ? a.nlse2[stat] : -INFINITY, valid ? a.nlse2[stat] : -INFINITY);  // -LSE2, twice
+    const float nDv = valid ? a.nD[stat] : 0.f;
+    const uint64_t nD2 = f2(nDv, nDv);
     uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
     for (int t = 0; t < inf.cnt; ++t, ++tiles) {
       const uint32_t e = e_next;  // the next entry's load overlaps this tile's work
@@ -301,15 +302,18 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       uint32_t pk[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const float p0 = ex2_approx(fmaf(s[2 * k], sl2, -lse2));
-        const float p1 = ex2_approx(fmaf(s[2 * k + 1], sl2, -lse2));
+        const uint64_t xx = ffma2(f2(s[2 * k], s[2 * k + 1]), sl2x2, nl2);
+        const uint64_t pp = f2(ex2_approx(f2lo(xx)), ex2_approx(f2hi(xx)));
+        uint64_t dd;
         if (kDrop) {  // dS' = P (Z dP~ - kp D)
           const float z0 = ((kb[k >> 4] >> ((2 * k) & 31)) & 1u) ? dp[2 * k] : 0.f;
           const float z1 = ((kb[k >> 4] >> ((2 * k + 1) & 31)) & 1u) ? dp[2 * k + 1] : 0.f;
-          pk[k] = pack_bf16x2(p0 * (z0 - Dv), p1 * (z1 - Dv));
+          dd = fadd2(f2(z0, z1), nD2);
         } else {
-          pk[k] = pack_bf16x2(p0 * (dp[2 * k] - Dv), p1 * (dp[2 * k + 1] - Dv));
+          dd = fadd2(f2(dp[2 * k], dp[2 * k + 1]), nD2);
         }
+        const uint64_t ds = fmul2(pp, dd);
+        pk[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
       }
       // dS (bf16) into TMEM buffer db, this thread's 64 key columns = 32 packed columns
       const int db = tiles & 1;
@@ -420,7 +424,7 @@ struct Item {
 };
 
 // Per-step data the producer warp stages for the compute warps (ring slot b):
-// the 64 query rows' LSE (base 2) and D, and the step's class, first rows,
+// the 64 query rows' -LSE*log2(e) and -D, and the step's class, first rows,
 // query head, map head and segment.  The compute warps read only shared
 // memory; on a partial tile they evaluate the mask themselves.
 struct StepMeta {  // 64 bytes
@@ -559,8 +563,8 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                 const int i = r0 + qi;
                 const uint32_t nb = (i < sg.q_len) ? 4u : 0u;
                 const size_t src = row0 + ((i < sg.q_len) ? i : 0);
-                cp_async_4(sl + qi, a.lse2 + src, nb);
-                cp_async_4(sd + qi, a.D + src, nb);
+                cp_async_4(sl + qi, a.nlse2 + src, nb);
+                cp_async_4(sd + qi, a.nD + src, nb);
               }
               cp_async_mbar_arrive_noinc(&bar[B_MFULL + b]);
               if (lane == 0) {
@@ -691,6 +695,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   const int j = wq * 32 + lane;  // key row inside the tile = TMEM lane
   const uint32_t tl = static_cast<uint32_t>(wq * 32) << 16;
   const float sl2 = a.scale_log2;
+  const uint64_t sl2x2 = f2(sl2, sl2);
   __nv_bfloat16* dK = static_cast<__nv_bfloat16*>(a.dk);
   __nv_bfloat16* dV = static_cast<__nv_bfloat16*>(a.dv);
   uint32_t steps = 0, acc_items = 0;
@@ -705,8 +710,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     for (int p = 0; p < inf.nsteps; ++p, ++steps) {
       const int b = steps & 1, r = steps % kRing;
       if (!waitw(&bar[B_MFULL + r], (steps / kRing) & 1, a, 234)) return;
-      const float* s_lse2 = stat_lse2(sm, r);
-      const float* s_D = stat_D(sm, r);
+      const float* s_nlse2 = stat_lse2(sm, r);
+      const float* s_nD = stat_D(sm, r);
       const StepMeta* meta_s = stat_meta(sm, r);
       const int cls = meta_s->cls;
       // mask bits of a partial tile, bit k = query 32*half + k for this
@@ -750,18 +755,22 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         for (int k = 0; k < 32; ++k) sv[k] = ((mb >> k) & 1u) ? sv[k] : -INFINITY;
       }
       uint32_t pp[16], pd[16];
+      // the staged statistics of this thread's 32 queries as packed pairs
+      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s_nlse2 + 32 * half);
+      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s_nD + 32 * half);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        const int q0 = 32 * half + 2 * k;
-        const float p0 = ex2_approx(fmaf(sv[2 * k], sl2, -s_lse2[q0]));
-        const float p1 = ex2_approx(fmaf(sv[2 * k + 1], sl2, -s_lse2[q0 + 1]));
+        const uint64_t xx = ffma2(f2(sv[2 * k], sv[2 * k + 1]), sl2x2, nl2[k]);
+        const float p0 = ex2_approx(f2lo(xx)), p1 = ex2_approx(f2hi(xx));
         if (kDrop) {  // P~ = P Z for dV; dS' = P Z dP~ - P kp D for dK
           const float pz0 = ((kb >> (2 * k)) & 1u) ? p0 : 0.f, pz1 = ((kb >> (2 * k + 1)) & 1u) ? p1 : 0.f;
           pp[k] = pack_bf16x2(pz0, pz1);
-          pd[k] = pack_bf16x2(fmaf(pz0, dp[2 * k], -p0 * s_D[q0]), fmaf(pz1, dp[2 * k + 1], -p1 * s_D[q0 + 1]));
+          const uint64_t pnd = fmul2(f2(p0, p1), nd2[k]);
+          pd[k] = pack_bf16x2(fmaf(pz0, dp[2 * k], f2lo(pnd)), fmaf(pz1, dp[2 * k + 1], f2hi(pnd)));
         } else {
           pp[k] = pack_bf16x2(p0, p1);
-          pd[k] = pack_bf16x2(p0 * (dp[2 * k] - s_D[q0]), p1 * (dp[2 * k + 1] - s_D[q0 + 1]));
+          const uint64_t ds = fmul2(f2(p0, p1), fadd2(f2(dp[2 * k], dp[2 * k + 1]), nd2[k]));
+          pd[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
         }
       }
       __syncwarp();

@@ -77,8 +77,9 @@ struct MergeArgs {
   int Tq, Hq;
 };
 void launch_merge(const MergeArgs& m, cudaStream_t st);
-// D = dmul * rowsum(dO * O): dmul is the keep probability under dropout, 1 otherwise.
-void launch_d_prepass(const void* o, const void* dout, const float* lse, float* D, float* lse2, int Tq, int Hq,
+// nD = -dmul * rowsum(dO * O) (dmul is the keep probability under dropout, 1
+// otherwise) and nlse2 = -LSE * log2(e) (-inf for rows with no key).
+void launch_d_prepass(const void* o, const void* dout, const float* lse, float* nD, float* nlse2, int Tq, int Hq,
                       float dmul, cudaStream_t st);
 void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream_t st);
 void launch_probe_timeout(int* status, unsigned long long limit_ns, cudaStream_t st);
@@ -115,8 +116,8 @@ struct AttnArgs {
   // tensors
   void* o;
   float* lse;
-  const float* D;
-  const float* lse2;
+  const float* nD;     // -D (times the keep probability under dropout), [Hq][Tq]
+  const float* nlse2;  // -LSE * log2(e), [Hq][Tq]
   void* dq;
   void* dk;
   void* dv;

@@ -479,10 +479,12 @@ void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uin
 
 // ---------------------------------------------------------------- D prepass
 // One block per (head, 64 rows).  Each half-warp reads one 256-byte row of O
-// and of dO (16 lanes x 16 bytes), so every load is a full sector.
+// and of dO (16 lanes x 16 bytes), so every load is a full sector.  Both
+// statistics are written negated (-dmul * D, -LSE * log2 e), the form in which
+// the backward kernels add them.
 __global__ void __launch_bounds__(256) d_prepass_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                                                        const float* __restrict__ lse, float* __restrict__ D,
-                                                        float* __restrict__ lse2, int Tq, int Hq, float dmul) {
+                                                        const float* __restrict__ lse, float* __restrict__ nD,
+                                                        float* __restrict__ nlse2, int Tq, int Hq, float dmul) {
   const int h = blockIdx.y;
   const int t0 = blockIdx.x * 64;
   const int hw = threadIdx.x >> 4;  // half-warp 0..15
@@ -523,21 +525,21 @@ __global__ void __launch_bounds__(256) d_prepass_kernel(const uint4* __restrict_
       const int t = t0 + it * 16 + hw;
       if (t < Tq) {
         const size_t idx = static_cast<size_t>(h) * Tq + t;
-        D[idx] = acc[it] * dmul;
+        nD[idx] = -(acc[it] * dmul);
         const float l = lse[idx];
-        // log2-domain LSE; a row with no key (-inf) gets +inf so that P = 0
-        lse2[idx] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+        // negated log2-domain LSE; a row with no key (LSE -inf) gets -inf so that P = 0
+        nlse2[idx] = (l == -INFINITY) ? -INFINITY : -(l * 1.4426950408889634f);
       }
     }
   }
 }
 
-void launch_d_prepass(const void* o, const void* dout, const float* lse, float* D, float* lse2, int Tq, int Hq,
+void launch_d_prepass(const void* o, const void* dout, const float* lse, float* nD, float* nlse2, int Tq, int Hq,
                       float dmul, cudaStream_t st) {
   if (Tq == 0) return;
   dim3 grid((Tq + 63) / 64, Hq);
   note_launches(1);
-  d_prepass_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, D, lse2,
+  d_prepass_kernel<<<grid, 256, 0, st>>>(static_cast<const uint4*>(o), static_cast<const uint4*>(dout), lse, nD, nlse2,
                                          Tq, Hq, dmul);
 }
 
