@@ -404,7 +404,7 @@ constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kTile128;
 constexpr int kOffQ = kOffV + kTile128;          // ring of 64-row Q tiles
 constexpr int kOffDO = kOffQ + kRing * kTile64;  // ring of 64-row dO tiles
-constexpr int kOffStat = kOffDO + kRing * kTile64;  // kRing buffers of: lse2[64], D[64], meta
+constexpr int kOffStat = kOffDO + kRing * kTile64;  // kRing buffers of: -LSE*log2e[64], -D[64], meta
 constexpr int kStatBytes = 64 * 4 * 2 + 64;
 constexpr int kOffCtl = kOffStat + kRing * kStatBytes;
 constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
@@ -436,12 +436,12 @@ struct StepMeta {  // 64 bytes
   int pad0, pad1, pad2;
   SegInfo sg;
 };
-__device__ __forceinline__ float* stat_lse2(uint8_t* sm, int b) {
+__device__ __forceinline__ float* stat_nlse2(uint8_t* sm, int b) {
   return reinterpret_cast<float*>(sm + kOffStat + b * kStatBytes);
 }
-__device__ __forceinline__ float* stat_D(uint8_t* sm, int b) { return stat_lse2(sm, b) + 64; }
+__device__ __forceinline__ float* stat_nD(uint8_t* sm, int b) { return stat_nlse2(sm, b) + 64; }
 __device__ __forceinline__ StepMeta* stat_meta(uint8_t* sm, int b) {
-  return reinterpret_cast<StepMeta*>(stat_lse2(sm, b) + 128);
+  return reinterpret_cast<StepMeta*>(stat_nlse2(sm, b) + 128);
 }
 
 // The whole producer warp runs this loop; lane 0 issues the TMA copies and
@@ -553,8 +553,8 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
               const int b = steps % kRing;
               const uint32_t reuse = steps / kRing;  // how many times ring slot b was filled before
               if (reuse >= 1 && !waitw(&bar[B_MEMPTY + b], (reuse - 1) & 1, a, 213)) goto abort;
-              float* sl = stat_lse2(sm, b);
-              float* sd = stat_D(sm, b);
+              float* sl = stat_nlse2(sm, b);
+              float* sd = stat_nD(sm, b);
               const size_t row0 = static_cast<size_t>(h) * pv.Tq + sg.q_off;
 #pragma unroll
               for (int u = 0; u < 2; ++u) {
@@ -710,8 +710,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     for (int p = 0; p < inf.nsteps; ++p, ++steps) {
       const int b = steps & 1, r = steps % kRing;
       if (!waitw(&bar[B_MFULL + r], (steps / kRing) & 1, a, 234)) return;
-      const float* s_nlse2 = stat_lse2(sm, r);
-      const float* s_nD = stat_D(sm, r);
+      const float* s_nlse2 = stat_nlse2(sm, r);
+      const float* s_nD = stat_nD(sm, r);
       const StepMeta* meta_s = stat_meta(sm, r);
       const int cls = meta_s->cls;
       // mask bits of a partial tile, bit k = query 32*half + k for this
