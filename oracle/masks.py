@@ -5,8 +5,8 @@ The LongCA-bench review ("Long-Context Attention Benchmark", section ä¸‰ æŠ€æœ¯æ
 FULL/CAUSAL DOCUMENT, SHARED QUESTION, GLOBAL SLIDING, CAUSAL BLOCKWISE,
 PREFIX LM CAUSAL, PREFIX LM DOCUMENT, BLOCK CAUSAL DOCUMENT) and 2 dynamic
 block masks (uniform blocks such as 64x64; variable-size blocks), but defines
-none of them.  The predicates below are the plainest readings; each reading is
-listed in DESIGN.md.
+none of them.  The predicates below (one branch per family in segment_mask)
+are the plainest readings of the family names and their parameters.
 
 Positions are relative to a segment: query row i in [0, q_len), key j in
 [0, k_len).  When q_len != k_len the causal diagonal is aligned bottom-right:
