@@ -200,9 +200,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
             umma_ss(tbase + 128, desc_add(dOd, off), desc_add(dV, off), kIdesc128, ks > 0);
           }
           umma_commit(&bar[B_SFULL]);
-          umma_commit(&bar[B_VEMPTY + vr]);
           ++sdp;
-          if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
         }
         if (t >= 1) {  // dQ += dS K for key tile t-1, dS read from TMEM
           const uint32_t idx = tiles + t - 1;
@@ -219,6 +217,11 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
           umma_commit(&bar[B_DSEMPTY + db]);
           umma_commit(&bar[B_KEMPTY + kr]);
           if (t == n) umma_commit(&bar[B_DQFULL]);
+        }
+        if (t < n) {  // the V and Q/dO releases of tile t wait until after the dQ group, so
+                      // that only the S/dP commit sits between the two MMA groups
+          umma_commit(&bar[B_VEMPTY + (tiles + t) % kVRing]);
+          if (t == n - 1) umma_commit(&bar[B_QEMPTY]);
         }
       }
       if (n == 0) umma_commit(&bar[B_QEMPTY]);
