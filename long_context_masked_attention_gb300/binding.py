@@ -245,6 +245,27 @@ def _workspace(call, for_bwd, workspace, device):
 
 
 # ------------------------------------------------------------------ entry points
+def _require(t, name, shape, dtype, device=None):
+    """The library reads and writes raw device pointers, so every tensor is
+    checked here: a CUDA tensor of the given dtype, shape and device, laid out
+    densely (a host or strided tensor would be read as garbage)."""
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t
+
+
 def _dropout(dropout):
     """(seed, p) -> lca_dropout, or None."""
     if dropout is None:
@@ -261,11 +282,14 @@ def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=N
 
     Tq, Hq, d = q.shape
     Tk, Hkv, _ = k.shape
+    bf = torch.bfloat16
+    _require(q, "q", (Tq, Hq, d), bf)
+    _require(k, "k", (Tk, Hkv, d), bf, q.device)
+    _require(v, "v", (Tk, Hkv, d), bf, q.device)
     call = call or marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale, q.device)
-    if out is None:
-        out = torch.empty_like(q)
-    if lse is None:
-        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    out = torch.empty_like(q) if out is None else _require(out, "out", (Tq, Hq, d), bf, q.device)
+    lse = (torch.empty((Hq, Tq), dtype=torch.float32, device=q.device) if lse is None
+           else _require(lse, "lse", (Hq, Tq), torch.float32, q.device))
     workspace = _workspace(call, False, workspace, q.device)
     drop = _dropout(dropout)
     if drop is None:
@@ -335,8 +359,12 @@ def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
     if n != len(lse_parts):
         raise ValueError("o_parts and lse_parts differ in length")
     Tq, Hq, d = o_parts[0].shape
-    out = torch.empty_like(o_parts[0]) if out is None else out
-    lse = torch.empty_like(lse_parts[0]) if lse is None else lse
+    dev = o_parts[0].device
+    for p, (o_p, l_p) in enumerate(zip(o_parts, lse_parts)):
+        _require(o_p, f"o_parts[{p}]", (Tq, Hq, d), torch.bfloat16, dev if p else None)
+        _require(l_p, f"lse_parts[{p}]", (Hq, Tq), torch.float32, dev)
+    out = torch.empty_like(o_parts[0]) if out is None else _require(out, "out", (Tq, Hq, d), torch.bfloat16, dev)
+    lse = torch.empty_like(lse_parts[0]) if lse is None else _require(lse, "lse", (Hq, Tq), torch.float32, dev)
     optrs = (C.c_void_p * n)(*[t.data_ptr() for t in o_parts])
     lptrs = (C.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
     _check(load().lca_attn_merge(optrs, lptrs, n, C.c_void_p(out.data_ptr()), C.c_void_p(lse.data_ptr()), Tq, Hq, d,
@@ -351,10 +379,17 @@ def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, d
 
     Tq, Hq, d = q.shape
     Tk, Hkv, _ = k.shape
+    bf = torch.bfloat16
+    _require(q, "q", (Tq, Hq, d), bf)
+    for name, t in (("do", do), ("o", o)):
+        _require(t, name, (Tq, Hq, d), bf, q.device)
+    _require(k, "k", (Tk, Hkv, d), bf, q.device)
+    _require(v, "v", (Tk, Hkv, d), bf, q.device)
+    _require(lse, "lse", (Hq, Tq), torch.float32, q.device)
     call = call or marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale, q.device)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq = torch.empty_like(q) if dq is None else _require(dq, "dq", (Tq, Hq, d), bf, q.device)
+    dk = torch.empty_like(k) if dk is None else _require(dk, "dk", (Tk, Hkv, d), bf, q.device)
+    dv = torch.empty_like(v) if dv is None else _require(dv, "dv", (Tk, Hkv, d), bf, q.device)
     workspace = _workspace(call, True, workspace, q.device)
     drop = _dropout(dropout)
     args = (do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(),

@@ -160,3 +160,24 @@ def test_dropout_entry_points_validate_like_the_plain_ones(L):
     bad = B.marshal(256, 256, 6, 4, 128, [Segment(0, 256, 0, 256)], MaskSpec("CAUSAL"))  # Hq % Hkv != 0
     assert L.lca_attn_fwd_dropout(fake, fake, fake, fake, fake, C.byref(bad.shape), C.byref(bad.mask),
                                   C.byref(drop), C.c_void_p(0x10000), 1 << 30, None) == 1
+
+
+def test_binding_rejects_unsuitable_tensors_before_calling_the_library():
+    """The binding hands raw device pointers to the library, so host, wrongly
+    typed, misshapen or strided tensors are rejected first (no CUDA needed)."""
+    import torch
+
+    segs, mask = [Segment(0, 8, 0, 8)], MaskSpec("CAUSAL")
+    q = torch.zeros(8, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        lib.attn_fwd(q, q[:, :1], q[:, :1], segs, mask)
+    with pytest.raises(ValueError, match="CUDA"):
+        lib.attn_bwd(q, q, q[:, :1], q[:, :1], q, torch.zeros(2, 8), segs, mask)
+    with pytest.raises(ValueError, match="CUDA"):
+        lib.attn_merge([q], [torch.zeros(2, 8)])
+    with pytest.raises(TypeError):
+        lib.attn_fwd(np.zeros((8, 2, 128)), q, q, segs, mask)
+    # the checks themselves, on tensor metadata only
+    meta = torch.empty(8, 2, 128, dtype=torch.bfloat16, device="meta")
+    with pytest.raises(ValueError, match="CUDA"):
+        B._require(meta, "q", (8, 2, 128), torch.bfloat16)

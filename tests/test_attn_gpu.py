@@ -128,3 +128,27 @@ def test_split_dkv_deterministic(lca):
     g2 = run_bwd(lca, prob, q, k, v, do, o, lse)
     for a, b in zip(g1, g2):
         assert np.array_equal(to_np(a), to_np(b))
+
+
+def test_binding_rejects_wrong_cuda_tensors(lca):
+    """Wrong dtype, shape, layout or device of a CUDA tensor is refused before
+    the library sees its pointer."""
+    import torch
+
+    from gen import MaskSpec, Segment
+
+    segs, mask = [Segment(0, 256, 0, 256)], MaskSpec("CAUSAL")
+    q = torch.randn(256, 4, 128, device="cuda").bfloat16()
+    k = torch.randn(256, 2, 128, device="cuda").bfloat16()
+    with pytest.raises(ValueError, match="dtype"):
+        lca.attn_fwd(q.float(), k, k, segs, mask)
+    with pytest.raises(ValueError, match="shape"):
+        lca.attn_fwd(q, k, k[:128], segs, mask)
+    with pytest.raises(ValueError, match="contiguous"):
+        lca.attn_fwd(q, k, k.transpose(0, 1).contiguous().transpose(0, 1), segs, mask)
+    with pytest.raises(ValueError, match="CUDA"):
+        lca.attn_fwd(q, k, k.cpu(), segs, mask)
+    o, lse = lca.attn_fwd(q, k, k, segs, mask)
+    with pytest.raises(ValueError, match="dtype"):
+        lca.attn_bwd(q, q, k, k, o, lse.double(), segs, mask)
+    torch.cuda.synchronize()
