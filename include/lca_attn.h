@@ -231,9 +231,12 @@ LCA_API lca_status lca_cad_plan(const int32_t* doc_len, int32_t n_docs, int32_t 
 LCA_API lca_status lca_mask_materialize(const lca_shape* shape, const lca_mask_desc* mask, int32_t head, int32_t seg,
                                 uint8_t* out, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Test hook: the tile classes (0 empty, 1 full, 2 partial) of one segment and
- * query head for 128 x 128 tiles, written to `out` (device, nq*nk bytes,
- * nq = ceil(q_len/128), nk = ceil(k_len/128)). */
+/* Test hook: the tile classes of one segment and query head for 128 x 128
+ * tiles, one byte per tile written to `out` (device, nq*nk bytes, row-major,
+ * nq = ceil(q_len/128), nk = ceil(k_len/128)).  Bits 0-1: 0 empty, 1 full,
+ * 2 partial.  A partial tile also sets bit 2 when its query rows [0, 64)
+ * attend no key of the tile, bit 3 when its rows [64, 128) (those inside the
+ * segment) attend none; the backward key-gradient pass skips those halves. */
 LCA_API lca_status lca_mask_tile_classes(const lca_shape* shape, const lca_mask_desc* mask, int32_t head, int32_t seg,
                                  uint8_t* out, void* workspace, size_t workspace_bytes, void* stream);
 

@@ -454,7 +454,7 @@ __device__ __forceinline__ StepMeta* stat_meta(uint8_t* sm, int b) {
 //
 // Steps of an item: for each query head of the KV head, each entry of its
 // list, each 64-row half of the 128-row query tile that lies inside the
-// segment.
+// segment and holds an attended cell.
 template <bool kCols>
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
@@ -545,9 +545,10 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
             const int ey = __shfl_sync(0xFFFFFFFFu, en.y, t);
             const int qt = ey & 0xFFFFFF;
             const uint32_t cls = static_cast<uint32_t>(ey >> 24) & 3u;
+            const uint32_t skip = static_cast<uint32_t>(ey >> 26) & 3u;  // bit h: half h attends nothing
             for (int half = 0; half < 2; ++half) {
               const int r0 = qt * kTile + 64 * half;
-              if (r0 >= sg.q_len) continue;
+              if (r0 >= sg.q_len || ((skip >> half) & 1u)) continue;
               if (us < inf.begin || us >= us_end) {  // outside this chunk
                 ++us;
                 continue;

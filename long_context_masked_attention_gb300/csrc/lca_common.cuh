@@ -36,6 +36,9 @@ enum MaskKind : int {
 };
 
 enum TileClass : uint32_t { kTileEmpty = 0, kTileFull = 1, kTilePartial = 2 };
+// Flags a PARTIAL tile's class byte may carry above its class (bits 0-1): no
+// attended cell in query rows [0, 64) / [64, 128) of the tile.
+constexpr uint32_t kHalf0Empty = 4, kHalf1Empty = 8;
 
 // Status codes written to the device status word (mirror lca_status).
 constexpr int kStatusTimeout = 5;
@@ -290,40 +293,53 @@ __device__ __forceinline__ uint32_t mask_bits_any(const MaskCtx& m, const SegInf
 
 // Class of the 128x128 tile with rows [r0, r0+128) and keys [c0, c0+128) of
 // one segment: EMPTY if no valid cell is attended, FULL if the tile lies
-// inside the segment and every cell is attended, PARTIAL otherwise.  All 32
-// lanes of the warp must call it; every lane gets the result.
+// inside the segment and every cell is attended, PARTIAL otherwise.  A
+// PARTIAL tile also carries kHalf0Empty / kHalf1Empty when no cell of its
+// rows [r0, r0+64) / [r0+64, r0+128) inside the segment is attended (the
+// dK/dV kernel skips such 64-row steps).  All 32 lanes of the warp must call
+// it; every lane gets the result.
 __device__ __forceinline__ uint32_t classify_tile_warp(const MaskCtx& m, const SegInfo& sg, int hm, int r0, int c0) {
   const int lane = threadIdx.x & 31;
   const int r1 = min(r0 + kTile, sg.q_len), c1 = min(c0 + kTile, sg.k_len);
   if (r1 <= r0 || c1 <= c0) return kTileEmpty;
   const bool inside = (r0 + kTile <= sg.q_len) && (c0 + kTile <= sg.k_len);
-  bool any = false, all = true;
+  const int rm = min(r0 + kTile / 2, r1);  // first row of the second half (r1 if it has none)
+  bool any0 = false, any1 = false, all = true;
   if (is_block_sparse(m.kind)) {
     const int qbA = q_block_of(m, sg.q_off + r0), qbB = q_block_of(m, sg.q_off + r1 - 1);
     const int kbA = k_block_of(m, sg.k_off + c0), kbB = k_block_of(m, sg.k_off + c1 - 1);
+    const int qbM0 = q_block_of(m, sg.q_off + rm - 1);                    // last block of half 0
+    const int qbM1 = (rm < r1) ? q_block_of(m, sg.q_off + rm) : qbB + 1;  // first block of half 1
     const int nq = qbB - qbA + 1, nk = kbB - kbA + 1;
     for (int t = lane; t < nq * nk; t += 32) {
-      const bool kept = block_kept(m, hm, qbA + t / nk, kbA + t % nk);
-      any |= kept;
+      const int qb = qbA + t / nk;
+      const bool kept = block_kept(m, hm, qb, kbA + t % nk);
+      any0 |= kept && qb <= qbM0;
+      any1 |= kept && qb >= qbM1;
       all &= kept;
     }
   } else if (m.kind == kFlashMask) {
     for (int c = c0 + lane; c < c1; c += 32) {
-      const int masked = col_masked_rows(__ldg(m.cols + sg.k_off + c), r0, r1);
-      any |= masked < r1 - r0;
-      all &= masked == 0;
+      const int4 b = __ldg(m.cols + sg.k_off + c);
+      const int masked0 = col_masked_rows(b, r0, rm), masked1 = col_masked_rows(b, rm, r1);
+      any0 |= masked0 < rm - r0;
+      any1 |= masked1 < r1 - rm;
+      all &= masked0 == 0 && masked1 == 0;
     }
   } else {
     for (int r = r0 + lane; r < r1; r += 32) {
       const Span s = row_span(m, sg, r);
-      any |= span_hits(s, c0, c1);
+      const bool hit = span_hits(s, c0, c1);
+      if (r < rm) any0 |= hit; else any1 |= hit;
       all &= span_covers(s, c0, c1);
     }
   }
-  any = __any_sync(0xFFFFFFFFu, any);
+  any0 = __any_sync(0xFFFFFFFFu, any0);
+  any1 = __any_sync(0xFFFFFFFFu, any1);
   all = __all_sync(0xFFFFFFFFu, all);
-  if (!any) return kTileEmpty;
-  return (all && inside) ? kTileFull : kTilePartial;
+  if (!any0 && !any1) return kTileEmpty;
+  if (all && inside) return kTileFull;
+  return kTilePartial | (any0 ? 0u : kHalf0Empty) | (any1 ? 0u : kHalf1Empty);
 }
 
 }  // namespace lca

@@ -126,8 +126,8 @@ __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls
     const int kt = k0 + lane;
     uint32_t c0 = 0, c1 = 0;
     if (kt < sg.nk) {
-      c0 = cls0[kt];
-      if (has1) c1 = cls0[sg.nk + kt];
+      c0 = cls0[kt] & 3u;  // the half-empty flags serve the 64-row dK/dV steps only
+      if (has1) c1 = cls0[sg.nk + kt] & 3u;
     }
     const uint32_t keep = __ballot_sync(0xFFFFFFFFu, (c0 | c1) != 0);
     if ((c0 | c1) != 0) out[n + __popc(keep & ((1u << lane) - 1u))] = static_cast<uint32_t>(kt) | (c0 << 24) | (c1 << 26);
@@ -158,7 +158,9 @@ void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl,
 // ---------------------------------------------------------------- key-major lists
 // One warp per unit (map KV head gm, key group, key tile).  For a shared map
 // (H' = 1) the unit has one list; for per-head maps it has one list per query
-// head of the KV head.  Entry = {segment, query tile | class << 24}.
+// head of the KV head.  Entry = {segment, query tile | class byte << 24}; the
+// class byte keeps its half-empty flags, and a unit counts one step per
+// 64-row half that lies inside the segment and is not flagged empty.
 __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ ucnt,
                                      int* __restrict__ list_cnt, int* __restrict__ list_steps,
                                      int* __restrict__ usteps, int2* __restrict__ entries,
@@ -189,7 +191,7 @@ __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tc
         int my_steps = 0;
         if (c != 0) {
           out[n + __popc(keep & ((1u << lane) - 1u))] = make_int2(s, qt | static_cast<int>(c << 24));
-          my_steps = (qt * kTile + 64 < sg.q_len) ? 2 : 1;  // 64-row halves inside the segment
+          my_steps = ((c & kHalf0Empty) ? 0 : 1) + ((qt * kTile + 64 < sg.q_len && !(c & kHalf1Empty)) ? 1 : 0);
         }
         n += __popc(keep);
         steps += __reduce_add_sync(0xFFFFFFFFu, my_steps);
@@ -398,7 +400,7 @@ __global__ void tile_classes_kernel(PlanView pv, int seg, int hm, uint8_t* __res
   if (tile >= nq * sg.nk) return;
   const int qt = tile / sg.nk, kt = tile % sg.nk;
   const uint32_t c = classify_tile_warp(pv.mask, sg, hm, qt * kTile, kt * kTile);
-  if ((threadIdx.x & 31) == 0) out[tile] = static_cast<uint8_t>(c);
+  if ((threadIdx.x & 31) == 0) out[tile] = static_cast<uint8_t>(c);  // class and half-empty flags
 }
 
 // nnz: interval families and FlashMask — one thread per query row, grid.y = segment.

@@ -38,6 +38,17 @@ def _check_masks(lib, prob, heads):
             assert np.array_equal(got, want), f"{prob.name} head {h} seg {s}: {(got != want).sum()} cells differ"
 
 
+def _want_class(blk, inside):
+    """Class byte of one 128x128 tile of the oracle mask: 0 empty, 1 full,
+    2 partial, plus 4 / 8 on a partial tile whose first / second 64 query rows
+    attend nothing."""
+    if not blk.any():
+        return 0
+    if blk.all() and inside:
+        return 1
+    return 2 | (0 if blk[:64].any() else 4) | (0 if blk[64:].any() else 8)
+
+
 def _check_classes(lib, prob, heads):
     call = _call(lib, prob)
     for h in heads:
@@ -50,7 +61,7 @@ def _check_classes(lib, prob, heads):
                 for kt in range(cls.shape[1]):
                     blk = M[qt * 128:(qt + 1) * 128, kt * 128:(kt + 1) * 128]
                     inside = (qt + 1) * 128 <= seg.q_len and (kt + 1) * 128 <= seg.k_len
-                    want = 0 if not blk.any() else (1 if (blk.all() and inside) else 2)
+                    want = _want_class(blk, inside)
                     assert cls[qt, kt] == want, f"{prob.name} h{h} s{s} tile ({qt},{kt}): {cls[qt, kt]} != {want}"
 
 
@@ -92,8 +103,7 @@ def test_block_sparse_masks_bit_exact(lca, variant):
         for qt in range(0, 64, 7):
             for kt in range(0, 256, 5):
                 blk = M[qt * 128:(qt + 1) * 128, kt * 128:(kt + 1) * 128]
-                want = 0 if not blk.any() else (1 if blk.all() else 2)
-                assert got_cls[qt, kt] == want
+                assert got_cls[qt, kt] == _want_class(blk, True)
     nnz = lca.mask_nnz(call).cpu().numpy()
     for h in heads:
         assert nnz[h] == oracle.mask_row_counts(prob, h).sum()
