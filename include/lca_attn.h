@@ -298,6 +298,8 @@ LCA_API const char* lca_last_error_detail(void);
 LCA_API uint64_t lca_launch_count(void);
 
 LCA_API const char* lca_status_string(lca_status status);
+/* Library revision, 100 + n; n grows whenever an entry point's behaviour
+ * changes (102: lca_mask_tile_classes reports the empty-half flags). */
 LCA_API int32_t lca_version(void);
 
 #ifdef __cplusplus

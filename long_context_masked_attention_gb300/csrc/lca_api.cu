@@ -584,7 +584,7 @@ const char* lca_status_string(lca_status s) {
   return "unknown status";
 }
 
-int32_t lca_version(void) { return 101; }
+int32_t lca_version(void) { return 102; }
 
 lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases) {
   if (events && (n_events < 2 || (n_events & 1))) return LCA_ERR_INVALID_ARG;
