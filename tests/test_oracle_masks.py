@@ -71,3 +71,24 @@ def test_flashmask_worked_example():
     p = Problem("fm4", 4, 4, 1, 1, 8, [Segment(0, 4, 0, 4)], MaskSpec("FLASHMASK", col_bounds=cb), 1)
     want = np.array([[1, 0, 0, 1], [1, 1, 0, 0], [1, 1, 1, 0], [1, 1, 0, 1]], dtype=bool)
     assert np.array_equal(oracle.dense_mask(p), want)
+
+
+def test_small_parity_cases_have_empty_tile_halves():
+    """The small GPU parity cases include partial 128x128 tiles one of whose
+    64-row halves attends nothing (the halves the backward's dK/dV pass
+    skips), so that element-wise parity covers the skip."""
+    found = {}
+    for prob in cases.gpu_small_all():
+        n = 0
+        for s, seg in enumerate(prob.segments):
+            if seg.q_len == 0 or seg.k_len == 0:
+                continue
+            M = oracle.segment_mask(prob.mask, s, seg, 0)
+            for q0 in range(0, seg.q_len, 128):
+                for k0 in range(0, seg.k_len, 128):
+                    blk = M[q0:q0 + 128, k0:k0 + 128]
+                    if blk.any() and not blk.all() and blk.shape[0] > 64:
+                        n += int(not blk[:64].any()) + int(not blk[64:].any())
+        found[prob.name] = n
+    assert found["g_small_bsu64"] > 0
+    assert found["g_small_bsv"] > 0
