@@ -411,21 +411,27 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         # Through the public API with host buffers: each step copies its inputs in
-        # from pinned memory and every mask's O, LSE, dQ, dK, dV back out.  The
-        # library is asynchronous on the caller's streams, so the copies run on
-        # other streams: a step's inputs arrive in the other of two input sets
-        # while the previous step computes, and each mask's outputs (own device
-        # buffers) go out on one of four streams while the next masks compute
-        # (several streams let several copy engines work at once).  One timed
-        # region covers all steps, from the first input copy to the last output
-        # copy.
+        # from pinned memory and brings every mask's O, LSE, dQ, dK, dV out to
+        # pinned host memory.  The library is asynchronous on the caller's
+        # streams, so the copies run on other streams: a step's inputs arrive in
+        # the other of two input sets while the previous step computes.  With
+        # --e2e-outputs copy (default) all five outputs go to device buffers and
+        # are copied out; with mapped the backward stores dQ, dK, dV straight
+        # into the pinned host tensors through their device mapping (the ABI
+        # accepts mapped host outputs; on a GB300 the stores cross NVLink-C2C)
+        # and only O and LSE, which the backward reads, are copied.  The copies of a
+        # mask's outputs run on one of four streams while the next masks
+        # compute (several streams let several copy engines work at once).  One
+        # timed region covers all steps, from the first input copy to the last
+        # output byte.
         copy = torch.cuda.Stream()  # host -> device inputs
         outq = [torch.cuda.Stream() for _ in range(4)]  # device -> host outputs, round robin over masks
         hosts_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
         dev_in = [[torch.empty_like(t) for t in (q, k, v, do)] for _ in range(2)]
-        dev_out = [(torch.empty_like(q), torch.empty_like(lse), torch.empty_like(q), torch.empty_like(k),
-                    torch.empty_like(v)) for _ in probs]
-        host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs] for outs in dev_out]
+        mapped = args.e2e_outputs == "mapped"
+        dev_out = [(torch.empty_like(q), torch.empty_like(lse)) +
+                   (() if mapped else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))) for _ in probs]
+        host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, lse, q, k, v)] for _ in probs]
         h2d = sum(t.numel() * t.element_size() for t in hosts_in)
         d2h = sum(t.numel() * t.element_size() for outs in host_out for t in outs)
         ev_in_ready = [torch.cuda.Event() for _ in range(2)]
@@ -451,7 +457,8 @@ def run_ours(args):
             stream.wait_event(ev_in_ready[b])
             qq, kk, vv, dd = dev_in[b]
             for i, (p, c) in enumerate(zip(probs, calls)):
-                oo, ll, gq, gk, gv = dev_out[i]
+                oo, ll = dev_out[i][:2]
+                gq, gk, gv = host_out[i][2:] if mapped else dev_out[i][2:]
                 if s >= 1:
                     stream.wait_event(ev_out_free[i])  # last step's copy of these buffers is done
                 lca.attn_fwd(qq, kk, vv, p.segments, p.mask, p.scale, out=oo, lse=ll, workspace=ws, call=c)
@@ -474,9 +481,13 @@ def run_ours(args):
         e_ms, e_flops = aggregate(t0.elapsed_time(t1), step_flops * args.steps, world, dev)
         e2e = {"value": e_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
-               "copies": "inputs on one copy stream, double-buffered across steps; each mask's outputs on one of "
-                         "four copy streams (round robin), overlapped with compute; one timed region from the "
-                         "first input copy to the last output copy"}
+               "outputs": args.e2e_outputs,
+               "copies": ("inputs on one copy stream, double-buffered across steps; dQ, dK, dV stored by the "
+                          "kernels into mapped pinned host memory, " if mapped else
+                          "inputs on one copy stream, double-buffered across steps; ") +
+                         "each mask's O and LSE" + ("" if mapped else ", dQ, dK, dV") +
+                         " copied out on one of four copy streams (round robin), overlapped with compute; one timed "
+                         "region from the first input copy to the last output byte"}
 
     pk, pk_src = peaks()
     peak, peak_src = tensor_peak(pk, pk_src, clk)
@@ -578,6 +589,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-outputs", choices=["copy", "mapped"], default="copy",
+                    help="end-to-end leg: outputs copied out (default), or gradients stored by the kernels into "
+                         "mapped pinned host memory (slower on a GB300: the stores stall the backward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None, help="comma-separated mask kinds or problem names (partial runs)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep8k")

@@ -30,6 +30,15 @@
  *    device pointers; "host" pointers are read during the call only.  The
  *    library allocates no device memory: it takes a caller-provided
  *    workspace of at least lca_workspace_size() bytes, 256-byte aligned.
+ *  - The outputs of lca_attn_fwd (o, lse) and lca_attn_bwd (dq, dk, dv) may
+ *    also be page-locked host memory that CUDA maps for the device
+ *    (cudaMallocHost, cudaHostAlloc, or cudaHostRegister with mapping): the
+ *    kernels store the results into it directly, which on a GB300 goes over
+ *    NVLink-C2C to the Grace host's memory and needs no copy afterwards.
+ *    Inputs and the workspace must be device (or managed) memory.  The
+ *    library asks CUDA what each pointer is before launching: a pointer of
+ *    another kind (pageable host memory, an unknown address) makes the call
+ *    return LCA_ERR_INVALID_ARG (LCA_ERR_WORKSPACE for the workspace).
  *  - Calls are asynchronous on `stream` and never synchronise, except
  *    lca_read_status.  Argument errors are returned before anything is
  *    launched.  Faults detected on the device (a bounded wait that ran out,
@@ -132,15 +141,15 @@ typedef struct {
 LCA_API lca_status lca_workspace_size(const lca_shape* shape, const lca_mask_desc* mask, int for_bwd, size_t* bytes);
 
 /* Forward (FlashAttention-2 核心优化: Q-split work, deferred rescale, one LSE
- * per row).  q, k, v: device bf16 inputs; o: device bf16 [Tq][Hq][d] output;
- * lse: device float [Hq][Tq] output. */
+ * per row).  q, k, v: device bf16 inputs; o: bf16 [Tq][Hq][d] output;
+ * lse: float [Hq][Tq] output (outputs in device or mapped host memory). */
 LCA_API lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward (FlashAttention-2 核心优化, 反向传播: dK/dV per key tile, dQ in a
  * separate query-tile pass, D = rowsum(dO * O) prepass).  dout, q, k, v, o:
- * device bf16; lse: device float from lca_attn_fwd; dq, dk, dv: device bf16
- * outputs (written, not accumulated). */
+ * device bf16; lse: device float from lca_attn_fwd; dq, dk, dv: bf16 outputs
+ * in device or mapped host memory (written, not accumulated). */
 LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
@@ -299,7 +308,8 @@ LCA_API uint64_t lca_launch_count(void);
 
 LCA_API const char* lca_status_string(lca_status status);
 /* Library revision, 100 + n; n grows whenever an entry point's behaviour
- * changes (102: lca_mask_tile_classes reports the empty-half flags). */
+ * changes (102: lca_mask_tile_classes reports the empty-half flags; 103:
+ * outputs may be mapped host memory, and every pointer's kind is checked). */
 LCA_API int32_t lca_version(void);
 
 #ifdef __cplusplus

@@ -245,17 +245,22 @@ def _workspace(call, for_bwd, workspace, device):
 
 
 # ------------------------------------------------------------------ entry points
-def _require(t, name, shape, dtype, device=None):
+def _require(t, name, shape, dtype, device=None, host_ok=False):
     """The library reads and writes raw device pointers, so every tensor is
     checked here: a CUDA tensor of the given dtype, shape and device, laid out
-    densely (a host or strided tensor would be read as garbage)."""
+    densely (a host or strided tensor would be read as garbage).  With
+    host_ok (outputs the kernels only store to), a pinned host tensor is
+    accepted too: the kernels write it through its device mapping."""
     import torch
 
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
-    if t.device.type != "cuda":
+    if host_ok and t.device.type == "cpu":
+        if not t.is_pinned():
+            raise ValueError(f"{name}: must be a CUDA tensor or a pinned host tensor (got unpinned {t.device})")
+    elif t.device.type != "cuda":
         raise ValueError(f"{name}: must be a CUDA tensor (got {t.device})")
-    if device is not None and t.device != device:
+    elif device is not None and t.device != device:
         raise ValueError(f"{name}: on {t.device}, expected {device}")
     if t.dtype != dtype:
         raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
@@ -277,6 +282,7 @@ def _dropout(dropout):
 def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=None, stream=None, call=None,
              dropout=None):
     """q [Tq,Hq,128], k/v [Tk,Hkv,128] bf16 CUDA tensors -> (o, lse[Hq,Tq]).
+    out / lse may be given as CUDA or pinned host tensors.
     dropout: (seed, p) for attention dropout with drop probability p."""
     import torch
 
@@ -287,9 +293,9 @@ def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=N
     _require(k, "k", (Tk, Hkv, d), bf, q.device)
     _require(v, "v", (Tk, Hkv, d), bf, q.device)
     call = call or marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale, q.device)
-    out = torch.empty_like(q) if out is None else _require(out, "out", (Tq, Hq, d), bf, q.device)
+    out = torch.empty_like(q) if out is None else _require(out, "out", (Tq, Hq, d), bf, q.device, host_ok=True)
     lse = (torch.empty((Hq, Tq), dtype=torch.float32, device=q.device) if lse is None
-           else _require(lse, "lse", (Hq, Tq), torch.float32, q.device))
+           else _require(lse, "lse", (Hq, Tq), torch.float32, q.device, host_ok=True))
     workspace = _workspace(call, False, workspace, q.device)
     drop = _dropout(dropout)
     if drop is None:
@@ -374,7 +380,8 @@ def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
 
 def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, dv=None, workspace=None, stream=None,
              call=None, dropout=None):
-    """Returns (dq, dk, dv) bf16.  dropout: the (seed, p) the forward used."""
+    """Returns (dq, dk, dv) bf16; given dq / dk / dv may be CUDA or pinned host
+    tensors.  dropout: the (seed, p) the forward used."""
     import torch
 
     Tq, Hq, d = q.shape
@@ -387,9 +394,9 @@ def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, d
     _require(v, "v", (Tk, Hkv, d), bf, q.device)
     _require(lse, "lse", (Hq, Tq), torch.float32, q.device)
     call = call or marshal(Tq, Tk, Hq, Hkv, d, segments, mask, scale, q.device)
-    dq = torch.empty_like(q) if dq is None else _require(dq, "dq", (Tq, Hq, d), bf, q.device)
-    dk = torch.empty_like(k) if dk is None else _require(dk, "dk", (Tk, Hkv, d), bf, q.device)
-    dv = torch.empty_like(v) if dv is None else _require(dv, "dv", (Tk, Hkv, d), bf, q.device)
+    dq = torch.empty_like(q) if dq is None else _require(dq, "dq", (Tq, Hq, d), bf, q.device, host_ok=True)
+    dk = torch.empty_like(k) if dk is None else _require(dk, "dk", (Tk, Hkv, d), bf, q.device, host_ok=True)
+    dv = torch.empty_like(v) if dv is None else _require(dv, "dv", (Tk, Hkv, d), bf, q.device, host_ok=True)
     workspace = _workspace(call, True, workspace, q.device)
     drop = _dropout(dropout)
     args = (do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(),

@@ -478,6 +478,34 @@ unsigned long long wait_limit_ns() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Inputs are read through TMA tensor maps and must be device (or managed)
+// memory.  Outputs are written with plain stores only, so they may also be
+// page-locked host memory that CUDA maps into the device's address space:
+// on a GB300 the kernels then store their results straight into the Grace
+// host's memory over NVLink-C2C.  `device_input` says whether `p` is memory
+// of the first kind; `output_address` returns the address the kernels use for
+// an output buffer, or nullptr for memory the device cannot reach (pageable
+// host memory, an unknown pointer), which the call refuses before launching.
+bool device_input(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+void* output_address(void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;  // null when not mapped for this device
+  return nullptr;
+}
+
 
 #define LCA_CUDA(x)                                  \
   do {                                               \
@@ -502,6 +530,7 @@ lca_status prepare(Call& c, const lca_shape* sh, const lca_mask_desc* md, void* 
   if (r != LCA_OK) return r;
   c.L = make_layout(c.P, fwd, bwd);
   if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0 || ws_bytes < c.L.total) return LCA_ERR_WORKSPACE;
+  if (!device_input(ws)) return LCA_ERR_WORKSPACE;  // counters and lists: device memory only
   c.ws = static_cast<uint8_t*>(ws);
   c.st = static_cast<cudaStream_t>(stream);
   c.V = make_view(c.P, c.L, c.ws);
@@ -584,7 +613,7 @@ const char* lca_status_string(lca_status s) {
   return "unknown status";
 }
 
-int32_t lca_version(void) { return 102; }
+int32_t lca_version(void) { return 103; }
 
 lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases) {
   if (events && (n_events < 2 || (n_events & 1))) return LCA_ERR_INVALID_ARG;
@@ -649,6 +678,13 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
   if (r != LCA_OK) return r;
   const HostPlan& P = c.P;
   if ((P.Tq > 0 && (!q || !o || !lse)) || (P.Tk > 0 && (!k || !v))) return LCA_ERR_INVALID_ARG;
+  if (P.Tq > 0) {
+    if (!device_input(q)) return LCA_ERR_INVALID_ARG;
+    o = output_address(o);
+    lse = static_cast<float*>(output_address(lse));
+    if (!o || !lse) return LCA_ERR_INVALID_ARG;
+  }
+  if (P.Tk > 0 && (!device_input(k) || !device_input(v))) return LCA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LCA_ERR_INVALID_ARG;
   const long long n_rows = static_cast<long long>(P.hm_count) * P.R256;
   CUtensorMap tq, tk, tv;
@@ -691,7 +727,7 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
   }
   const size_t row_bytes = static_cast<size_t>(P.Hq) * kHeadDim * 2;
   for (auto& gp : P.q_gaps) {
-    LCA_CUDA(cudaMemsetAsync(static_cast<uint8_t*>(o) + gp.first * row_bytes, 0, gp.second * row_bytes, c.st));
+    launch_zero16(static_cast<uint8_t*>(o) + gp.first * row_bytes, gp.second * row_bytes, c.st);
     launch_fill_lse(lse, P.Tq, P.Hq, gp.first, gp.second, c.st);
   }
   LCA_CUDA(cudaGetLastError());
@@ -746,6 +782,17 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
   const HostPlan& P = c.P;
   if ((P.Tq > 0 && (!dout || !q || !o || !lse || !dq)) || (P.Tk > 0 && (!k || !v || !dk || !dv)))
     return LCA_ERR_INVALID_ARG;
+  if (P.Tq > 0) {
+    if (!device_input(dout) || !device_input(q) || !device_input(o) || !device_input(lse)) return LCA_ERR_INVALID_ARG;
+    dq = output_address(dq);
+    if (!dq) return LCA_ERR_INVALID_ARG;
+  }
+  if (P.Tk > 0) {
+    if (!device_input(k) || !device_input(v)) return LCA_ERR_INVALID_ARG;
+    dk = output_address(dk);
+    dv = output_address(dv);
+    if (!dk || !dv) return LCA_ERR_INVALID_ARG;
+  }
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv))
     return LCA_ERR_INVALID_ARG;
@@ -851,11 +898,10 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     phase_end(ph, c.st);
   }
   const size_t qrow = static_cast<size_t>(P.Hq) * kHeadDim * 2, krow = static_cast<size_t>(P.Hkv) * kHeadDim * 2;
-  for (auto& gp : P.q_gaps)
-    LCA_CUDA(cudaMemsetAsync(static_cast<uint8_t*>(dq) + gp.first * qrow, 0, gp.second * qrow, c.st));
+  for (auto& gp : P.q_gaps) launch_zero16(static_cast<uint8_t*>(dq) + gp.first * qrow, gp.second * qrow, c.st);
   for (auto& gp : P.k_gaps) {
-    LCA_CUDA(cudaMemsetAsync(static_cast<uint8_t*>(dk) + gp.first * krow, 0, gp.second * krow, c.st));
-    LCA_CUDA(cudaMemsetAsync(static_cast<uint8_t*>(dv) + gp.first * krow, 0, gp.second * krow, c.st));
+    launch_zero16(static_cast<uint8_t*>(dk) + gp.first * krow, gp.second * krow, c.st);
+    launch_zero16(static_cast<uint8_t*>(dv) + gp.first * krow, gp.second * krow, c.st);
   }
   LCA_CUDA(cudaGetLastError());
   return LCA_OK;

@@ -82,6 +82,7 @@ void launch_merge(const MergeArgs& m, cudaStream_t st);
 void launch_d_prepass(const void* o, const void* dout, const float* lse, float* nD, float* nlse2, int Tq, int Hq,
                       float dmul, cudaStream_t st);
 void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream_t st);
+void launch_zero16(void* p, size_t bytes, cudaStream_t st);  // bytes a multiple of 16, p 16-byte aligned
 void launch_probe_timeout(int* status, unsigned long long limit_ns, cudaStream_t st);
 
 // ------------------------------------------------------------ attention kernels

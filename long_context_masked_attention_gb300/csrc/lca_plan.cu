@@ -612,6 +612,23 @@ void launch_fill_lse(float* lse, int Tq, int Hq, int row0, int nrows, cudaStream
   fill_lse_kernel<<<static_cast<int>((n + 255) / 256), 256, 0, st>>>(lse, Tq, Hq, row0, nrows);
 }
 
+// Zero `n16` 16-byte words from `p` with plain stores, so that the rows no
+// segment covers read as 0 in an output that may live in device memory or in
+// device-mapped page-locked host memory.
+__global__ void zero16_kernel(uint4* __restrict__ p, long long n16) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+void launch_zero16(void* p, size_t bytes, cudaStream_t st) {
+  const long long n16 = static_cast<long long>(bytes / 16);
+  if (n16 == 0) return;
+  note_launches(1);
+  const long long blocks = std::min<long long>((n16 + 255) / 256, 4096);
+  zero16_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(static_cast<uint4*>(p), n16);
+}
+
 // ---------------------------------------------------------------- timeout probe
 __global__ void probe_timeout_kernel(int* status, unsigned long long limit_ns) {
   __shared__ __align__(8) uint64_t bar;

@@ -181,3 +181,6 @@ def test_binding_rejects_unsuitable_tensors_before_calling_the_library():
     meta = torch.empty(8, 2, 128, dtype=torch.bfloat16, device="meta")
     with pytest.raises(ValueError, match="CUDA"):
         B._require(meta, "q", (8, 2, 128), torch.bfloat16)
+    # outputs may be pinned host tensors, never pageable ones
+    with pytest.raises(ValueError, match="pinned"):
+        B._require(q, "dq", (8, 2, 128), torch.bfloat16, host_ok=True)

@@ -152,3 +152,44 @@ def test_binding_rejects_wrong_cuda_tensors(lca):
     with pytest.raises(ValueError, match="dtype"):
         lca.attn_bwd(q, q, k, k, o, lse.double(), segs, mask)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["edge_gaps", "g_small_bsv"])
+def test_outputs_in_pinned_host_memory(lca, name):
+    """Outputs may be page-locked host tensors: the kernels store into them
+    through their device mapping (rows outside every segment included, which a
+    zero-fill kernel writes), bit for bit what device outputs receive.  A
+    pageable host output is refused, by the binding and by the library."""
+    import ctypes as C
+
+    import torch
+
+    prob = {p.name: p for p in cases.gpu_small_all() + cases.edge_cases()}[name]
+    q, k, v, do = (t.cuda() for t in make_tensors(prob))
+    segs, mask, sc = prob.segments, prob.mask, prob.scale
+    o, lse = lca.attn_fwd(q, k, v, segs, mask, sc)
+    dq, dk, dv = lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc)
+    torch.cuda.synchronize()
+
+    def pinned(t):
+        return torch.full(t.shape, 7, dtype=t.dtype, pin_memory=True)  # 7: stale contents must be overwritten
+
+    oh, lh = pinned(o), pinned(lse)
+    lca.attn_fwd(q, k, v, segs, mask, sc, out=oh, lse=lh)
+    gh = [pinned(t) for t in (dq, dk, dv)]
+    lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc, dq=gh[0], dk=gh[1], dv=gh[2])
+    torch.cuda.synchronize()
+    assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
+    for h, d in zip(gh, (dq, dk, dv)):
+        assert torch.equal(h, d.cpu())
+
+    pageable = torch.empty(dq.shape, dtype=dq.dtype)
+    with pytest.raises(ValueError, match="pinned"):
+        lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc, dq=pageable)
+    call = lca.marshal(prob.Tq, prob.Tk, prob.Hq, prob.Hkv, prob.d, segs, mask, sc)
+    ws = torch.empty(max(lca.workspace_size(call, True), 256), dtype=torch.uint8, device="cuda")
+    st = lca.binding.load().lca_attn_bwd(do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), pageable.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                         C.byref(call.shape), C.byref(call.mask), ws.data_ptr(), ws.numel(), None)
+    assert st == 1  # LCA_ERR_INVALID_ARG, returned before any launch
+    torch.cuda.synchronize()
