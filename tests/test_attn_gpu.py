@@ -154,30 +154,34 @@ def test_binding_rejects_wrong_cuda_tensors(lca):
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("name", ["edge_gaps", "g_small_bsv"])
-def test_outputs_in_pinned_host_memory(lca, name):
+HOST_OUT = [(p, None) for p in cases.edge_cases() + cases.gpu_small_all() if p.name in ("edge_gaps", "g_small_bsv")]
+HOST_OUT += [(SPLIT[0], None), (SPLIT[0], (5, 0.1))]
+
+
+@pytest.mark.parametrize("prob,drop", HOST_OUT, ids=[p.name + ("_drop" if d else "") for p, d in HOST_OUT])
+def test_outputs_in_pinned_host_memory(lca, prob, drop):
     """Outputs may be page-locked host tensors: the kernels store into them
-    through their device mapping (rows outside every segment included, which a
-    zero-fill kernel writes), bit for bit what device outputs receive.  A
-    pageable host output is refused, by the binding and by the library."""
+    through their device mapping (rows outside every segment, which a
+    zero-fill kernel writes, and the reduced chunks of split dK/dV units
+    included), bit for bit what device outputs receive.  A pageable host
+    output is refused, by the binding and by the library."""
     import ctypes as C
 
     import torch
 
-    prob = {p.name: p for p in cases.gpu_small_all() + cases.edge_cases()}[name]
     q, k, v, do = (t.cuda() for t in make_tensors(prob))
     segs, mask, sc = prob.segments, prob.mask, prob.scale
-    o, lse = lca.attn_fwd(q, k, v, segs, mask, sc)
-    dq, dk, dv = lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc)
+    o, lse = lca.attn_fwd(q, k, v, segs, mask, sc, dropout=drop)
+    dq, dk, dv = lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc, dropout=drop)
     torch.cuda.synchronize()
 
     def pinned(t):
         return torch.full(t.shape, 7, dtype=t.dtype, pin_memory=True)  # 7: stale contents must be overwritten
 
     oh, lh = pinned(o), pinned(lse)
-    lca.attn_fwd(q, k, v, segs, mask, sc, out=oh, lse=lh)
+    lca.attn_fwd(q, k, v, segs, mask, sc, out=oh, lse=lh, dropout=drop)
     gh = [pinned(t) for t in (dq, dk, dv)]
-    lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc, dq=gh[0], dk=gh[1], dv=gh[2])
+    lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc, dq=gh[0], dk=gh[1], dv=gh[2], dropout=drop)
     torch.cuda.synchronize()
     assert torch.equal(oh, o.cpu()) and torch.equal(lh, lse.cpu())
     for h, d in zip(gh, (dq, dk, dv)):
