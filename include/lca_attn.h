@@ -28,8 +28,14 @@
  *    outside every segment get dK = dV = 0.
  *  - The caller owns every buffer.  Pointers documented "device" are CUDA
  *    device pointers; "host" pointers are read during the call only.  The
- *    library allocates no device memory: it takes a caller-provided
- *    workspace of at least lca_workspace_size() bytes, 256-byte aligned.
+ *    calls allocate no device memory: they take a caller-provided workspace
+ *    of at least lca_workspace_size() bytes, 256-byte aligned.  (The one
+ *    static array of lca_attn_fwd_static_workspace is reserved by CUDA when
+ *    it loads this library's device code on a device; see there.)
+ *  - Every device pointer must belong to the device that is current when the
+ *    call is made (or be managed memory); the stream must belong to that
+ *    device too.  A pointer to another device's memory is refused with
+ *    LCA_ERR_INVALID_ARG before anything is launched.
  *  - The outputs of lca_attn_fwd (o, lse) and lca_attn_bwd (dq, dk, dv) may
  *    also be page-locked host memory that CUDA maps for the device
  *    (cudaMallocHost, cudaHostAlloc, or cudaHostRegister with mapping): the
@@ -267,8 +273,13 @@ LCA_API lca_status lca_mask_nnz(const lca_shape* shape, const lca_mask_desc* mas
  * shape whose forward workspace (lca_workspace_size with for_bwd = 0) is
  * larger is rejected with LCA_ERR_WORKSPACE before anything is launched, and
  * lca_last_error_detail says how much it needed.
- * The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.
+ * The array is reserved on a device when CUDA loads this library's device
+ * code there: with CUDA's default lazy loading that happens at the latest
+ * during the first call of this function on the device, which can then fail
+ * with LCA_ERR_CUDA if the device is already full.  Make that first call at
+ * set-up time, before the rest of device memory is handed out (a small shape
+ * will do); it also looks up the array's device address with that device
+ * current, so it must come before any stream capture.
  * Every call on a device shares the one array and clears what must start at
  * zero; calls that overlap on the GPU (two streams, or two host threads)
  * race on it, so the caller must serialise them.
@@ -309,7 +320,8 @@ LCA_API uint64_t lca_launch_count(void);
 LCA_API const char* lca_status_string(lca_status status);
 /* Library revision, 100 + n; n grows whenever an entry point's behaviour
  * changes (102: lca_mask_tile_classes reports the empty-half flags; 103:
- * outputs may be mapped host memory, and every pointer's kind is checked). */
+ * outputs may be mapped host memory, and every pointer's kind is checked;
+ * 104: device pointers of another device than the current one are refused). */
 LCA_API int32_t lca_version(void);
 
 #ifdef __cplusplus

@@ -220,12 +220,28 @@ def _check(code, what):
         raise LcaError(code, what)
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The stream handle for a call: the given one, else the current stream
+    of `device` (the device the call's tensors live on)."""
     import torch
 
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _on_device(device):
+    """Context that makes `device` the current CUDA device for a library call:
+    the library launches on the current device and refuses pointers into
+    another device's memory, so every call runs with its tensors' device
+    current, whichever device the caller had selected."""
+    import contextlib
+
+    import torch
+
+    if device is None or torch.device(device).type != "cuda":
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def workspace_size(call: Call, for_bwd: bool) -> int:
@@ -298,15 +314,16 @@ def attn_fwd(q, k, v, segments, mask, scale=0.0, out=None, lse=None, workspace=N
            else _require(lse, "lse", (Hq, Tq), torch.float32, q.device, host_ok=True))
     workspace = _workspace(call, False, workspace, q.device)
     drop = _dropout(dropout)
-    if drop is None:
-        _check(load().lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                   C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(), workspace.numel(),
-                                   _stream(stream)), "lca_attn_fwd")
-    else:
-        _check(load().lca_attn_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                                           C.byref(call.shape), C.byref(call.mask), C.byref(drop),
-                                           workspace.data_ptr(), workspace.numel(), _stream(stream)),
-               "lca_attn_fwd_dropout")
+    with _on_device(q.device):
+        if drop is None:
+            _check(load().lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       C.byref(call.shape), C.byref(call.mask), workspace.data_ptr(),
+                                       workspace.numel(), _stream(stream, q.device)), "lca_attn_fwd")
+        else:
+            _check(load().lca_attn_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                               lse.data_ptr(), C.byref(call.shape), C.byref(call.mask),
+                                               C.byref(drop), workspace.data_ptr(), workspace.numel(),
+                                               _stream(stream, q.device)), "lca_attn_fwd_dropout")
     return out, lse
 
 
@@ -373,8 +390,9 @@ def attn_merge(o_parts, lse_parts, out=None, lse=None, stream=None):
     lse = torch.empty_like(lse_parts[0]) if lse is None else _require(lse, "lse", (Hq, Tq), torch.float32, dev)
     optrs = (C.c_void_p * n)(*[t.data_ptr() for t in o_parts])
     lptrs = (C.c_void_p * n)(*[t.data_ptr() for t in lse_parts])
-    _check(load().lca_attn_merge(optrs, lptrs, n, C.c_void_p(out.data_ptr()), C.c_void_p(lse.data_ptr()), Tq, Hq, d,
-                                 _stream(stream)), "lca_attn_merge")
+    with _on_device(dev):
+        _check(load().lca_attn_merge(optrs, lptrs, n, C.c_void_p(out.data_ptr()), C.c_void_p(lse.data_ptr()), Tq, Hq,
+                                     d, _stream(stream, dev)), "lca_attn_merge")
     return out, lse
 
 
@@ -401,11 +419,12 @@ def attn_bwd(do, q, k, v, o, lse, segments, mask, scale=0.0, dq=None, dk=None, d
     drop = _dropout(dropout)
     args = (do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dq.data_ptr(),
             dk.data_ptr(), dv.data_ptr(), C.byref(call.shape), C.byref(call.mask))
-    tail = (workspace.data_ptr(), workspace.numel(), _stream(stream))
-    if drop is None:
-        _check(load().lca_attn_bwd(*args, *tail), "lca_attn_bwd")
-    else:
-        _check(load().lca_attn_bwd_dropout(*args, C.byref(drop), *tail), "lca_attn_bwd_dropout")
+    with _on_device(q.device):
+        tail = (workspace.data_ptr(), workspace.numel(), _stream(stream, q.device))
+        if drop is None:
+            _check(load().lca_attn_bwd(*args, *tail), "lca_attn_bwd")
+        else:
+            _check(load().lca_attn_bwd_dropout(*args, C.byref(drop), *tail), "lca_attn_bwd_dropout")
     return dq, dk, dv
 
 
@@ -414,8 +433,10 @@ def mask_materialize(call: Call, head: int, seg: int, q_len: int, k_len: int, de
 
     out = torch.empty((q_len, k_len), dtype=torch.uint8, device=device)
     ws = _workspace(call, False, None, device)
-    _check(load().lca_mask_materialize(C.byref(call.shape), C.byref(call.mask), head, seg, out.data_ptr(),
-                                       ws.data_ptr(), ws.numel(), _stream(stream)), "lca_mask_materialize")
+    with _on_device(out.device):
+        _check(load().lca_mask_materialize(C.byref(call.shape), C.byref(call.mask), head, seg, out.data_ptr(),
+                                           ws.data_ptr(), ws.numel(), _stream(stream, out.device)),
+               "lca_mask_materialize")
     return out
 
 
@@ -425,8 +446,10 @@ def mask_tile_classes(call: Call, head: int, seg: int, q_len: int, k_len: int, d
     nq, nk = -(-q_len // 128), -(-k_len // 128)
     out = torch.empty((max(nq, 0), max(nk, 0)), dtype=torch.uint8, device=device)
     ws = _workspace(call, False, None, device)
-    _check(load().lca_mask_tile_classes(C.byref(call.shape), C.byref(call.mask), head, seg, out.data_ptr(),
-                                        ws.data_ptr(), ws.numel(), _stream(stream)), "lca_mask_tile_classes")
+    with _on_device(out.device):
+        _check(load().lca_mask_tile_classes(C.byref(call.shape), C.byref(call.mask), head, seg, out.data_ptr(),
+                                            ws.data_ptr(), ws.numel(), _stream(stream, out.device)),
+               "lca_mask_tile_classes")
     return out
 
 
@@ -435,20 +458,24 @@ def mask_nnz(call: Call, device="cuda", stream=None):
 
     out = torch.zeros(call.shape.Hq, dtype=torch.int64, device=device)
     ws = _workspace(call, False, None, device)
-    _check(load().lca_mask_nnz(C.byref(call.shape), C.byref(call.mask), out.data_ptr(), ws.data_ptr(), ws.numel(),
-                               _stream(stream)), "lca_mask_nnz")
+    with _on_device(out.device):
+        _check(load().lca_mask_nnz(C.byref(call.shape), C.byref(call.mask), out.data_ptr(), ws.data_ptr(),
+                                   ws.numel(), _stream(stream, out.device)), "lca_mask_nnz")
     return out
 
 
 def read_status(workspace, stream=None):
     buf = (C.c_int32 * 2)()
-    _check(load().lca_read_status(workspace.data_ptr(), buf, _stream(stream)), "lca_read_status")
+    with _on_device(workspace.device):
+        _check(load().lca_read_status(workspace.data_ptr(), buf, _stream(stream, workspace.device)),
+               "lca_read_status")
     return int(buf[0]), int(buf[1])
 
 
 def probe_wait_timeout(workspace, limit_ms: int, stream=None):
-    _check(load().lca_probe_wait_timeout(workspace.data_ptr(), workspace.numel(), int(limit_ms), _stream(stream)),
-           "lca_probe_wait_timeout")
+    with _on_device(workspace.device):
+        _check(load().lca_probe_wait_timeout(workspace.data_ptr(), workspace.numel(), int(limit_ms),
+                                             _stream(stream, workspace.device)), "lca_probe_wait_timeout")
 
 
 class KernelEvents:

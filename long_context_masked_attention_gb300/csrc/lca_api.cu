@@ -482,17 +482,31 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // memory.  Outputs are written with plain stores only, so they may also be
 // page-locked host memory that CUDA maps into the device's address space:
 // on a GB300 the kernels then store their results straight into the Grace
-// host's memory over NVLink-C2C.  `device_input` says whether `p` is memory
-// of the first kind; `output_address` returns the address the kernels use for
-// an output buffer, or nullptr for memory the device cannot reach (pageable
-// host memory, an unknown pointer), which the call refuses before launching.
+// host's memory over NVLink-C2C.  Device memory must belong to the device
+// that is current for the call (the one the kernels run on): a pointer into
+// another GPU's memory would make the kernels fault or read across the link.
+// `device_input` says whether `p` is memory the kernels may read;
+// `output_address` returns the address the kernels use for an output
+// buffer, or nullptr for memory they must not write (another device's,
+// pageable host memory, an unknown pointer), which the call refuses before
+// launching.
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return dev;
+}
+
 bool device_input(const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return false;
   }
-  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+  if (at.type == cudaMemoryTypeManaged) return true;
+  return at.type == cudaMemoryTypeDevice && at.device == current_device();
 }
 
 void* output_address(void* p) {
@@ -501,8 +515,10 @@ void* output_address(void* p) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
-  if (at.type == cudaMemoryTypeHost) return at.devicePointer;  // null when not mapped for this device
+  if (at.type == cudaMemoryTypeManaged) return p;
+  if (at.type == cudaMemoryTypeDevice) return at.device == current_device() ? p : nullptr;
+  // mapped host memory: the address valid on the current device (null when not mapped for it)
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer;
   return nullptr;
 }
 
@@ -613,7 +629,7 @@ const char* lca_status_string(lca_status s) {
   return "unknown status";
 }
 
-int32_t lca_version(void) { return 103; }
+int32_t lca_version(void) { return 104; }
 
 lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases) {
   if (events && (n_events < 2 || (n_events & 1))) return LCA_ERR_INVALID_ARG;

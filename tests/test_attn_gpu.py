@@ -197,3 +197,35 @@ def test_outputs_in_pinned_host_memory(lca, prob, drop):
                                          C.byref(call.shape), C.byref(call.mask), ws.data_ptr(), ws.numel(), None)
     assert st == 1  # LCA_ERR_INVALID_ARG, returned before any launch
     torch.cuda.synchronize()
+
+
+def test_pointer_of_another_device_refused(lca):
+    """With cuda:0 current, a call whose tensors live on cuda:1 is refused
+    with LCA_ERR_INVALID_ARG before anything is launched (the kernels would
+    run on cuda:0 and read another GPU's memory); through the binding, which
+    makes the tensors' device current, the same call runs on cuda:1."""
+    import ctypes as C
+
+    import torch
+
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two visible GPUs")
+    from gen import MaskSpec, Segment
+
+    segs, mask = [Segment(0, 256, 0, 256)], MaskSpec("CAUSAL")
+    dev1 = torch.device("cuda", 1)
+    q = torch.randn(256, 4, 128, device=dev1).bfloat16()
+    k = torch.randn(256, 2, 128, device=dev1).bfloat16()
+    o, lse = torch.empty_like(q), torch.empty((4, 256), dtype=torch.float32, device=dev1)
+    call = lca.marshal(256, 256, 4, 2, 128, segs, mask)
+    ws = torch.empty(max(lca.workspace_size(call, False), 256), dtype=torch.uint8, device=dev1)
+    L = lca.binding.load()
+    with torch.cuda.device(0):
+        before = L.lca_launch_count()
+        code = L.lca_attn_fwd(q.data_ptr(), k.data_ptr(), k.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              C.byref(call.shape), C.byref(call.mask), ws.data_ptr(), ws.numel(), None)
+        assert code == 1
+        assert L.lca_launch_count() == before
+        o1, lse1 = lca.attn_fwd(q, k, k, segs, mask)
+    torch.cuda.synchronize(dev1)
+    assert o1.device == dev1 and torch.isfinite(lse1).all()

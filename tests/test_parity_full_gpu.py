@@ -4,18 +4,20 @@ can compute row by row, plus properties that hold at any size.
 
 Sampled, not exhaustive: for a few segments (largest, a middle one, the
 smallest) and query heads spread over the KV groups, the first, middle and
-last 64 rows get O, LSE and dQ checked; dK/dV are checked on the last key
-tile of causal segments (attended only by the segment's last rows, so the
-oracle can compute them exactly) and, everywhere, through the identities
+last 64 rows get O, LSE and dQ checked.  dK/dV are checked element-wise on
+chosen key tiles -- the first, an interior one, the last and one the mask
+makes partial -- against the oracle summed over every query head of the KV
+group and every row (of every segment) that attends those keys; at 48K and
+512K on documents no longer than 32K.  Everywhere, the identities
 sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i (over the query heads of each KV
-head), which hold for any mask because every softmax row sums to one."""
+head) hold for any mask because every softmax row sums to one."""
 from __future__ import annotations
 
 import numpy as np
 import pytest
 
 import oracle
-from gen import config3, config4, config5, make_tensors
+from gen import STATIC_KINDS, config2, config3, config4, config5, make_tensors
 from tests.gpu_util import FWD_MAX_ABS, FWD_MEAN_ABS, LSE_ABS, BWD_REL_L2, to_np
 
 pytestmark = pytest.mark.gpu
@@ -129,6 +131,156 @@ def _heads(prob):
     return sorted({0, G + 1 if prob.Hq > G + 1 else 0, prob.Hq - 1})
 
 
+def _one_head_per_group(prob):
+    """One query head of every KV group, at a different place in each group."""
+    G = prob.Hq // prob.Hkv
+    return [g * G + g % G for g in range(prob.Hkv)]
+
+
+def _oracle_key_tiles(prob, inputs, s, g, kts, chunk=1024):
+    """Oracle dK, dV of key tiles `kts` (128 keys each, relative to segment
+    s's keys) of KV head g: the sum over every segment that reads those keys
+    (the same k_off: shards of one document), every query head of the group
+    and every query row that attends at least one of the keys.  Rows that
+    attend none of them contribute nothing, so they are left out."""
+    seg = prob.segments[s]
+    cols = np.concatenate([np.arange(kt * 128, min(seg.k_len, kt * 128 + 128)) for kt in kts])
+    dK = np.zeros((cols.size, prob.d))
+    dV = np.zeros((cols.size, prob.d))
+    G = prob.Hq // prob.Hkv
+    for s2, seg2 in enumerate(prob.segments):
+        if seg2.k_off != seg.k_off or seg2.q_len == 0:
+            continue
+        sel = np.nonzero(cols < seg2.k_len)[0]
+        if sel.size == 0:
+            continue
+        for h in range(g * G, (g + 1) * G):
+            for r0 in range(0, seg2.q_len, chunk):
+                rows = np.arange(r0, min(seg2.q_len, r0 + chunk))
+                m = oracle.segment_mask(prob.mask, s2, seg2, h, rows)[:, cols[sel]]
+                att = rows[m.any(axis=1)]
+                if att.size == 0:
+                    continue
+                a, b = oracle.key_grads_from_rows(prob, *inputs, s2, h, att, cols[sel])
+                dK[sel] += a
+                dV[sel] += b
+    out, at = [], 0
+    for kt in kts:
+        n = min(seg.k_len, kt * 128 + 128) - kt * 128
+        out.append((dK[at:at + n], dV[at:at + n]))
+        at += n
+    return out
+
+
+def _check_key_tiles(prob, inputs, outputs, s, g, kts, what=""):
+    """dK/dV of the given key tiles of segment s, KV head g, element-wise
+    (relative L2 per tile) against the oracle."""
+    _, _, _, dk, dv = outputs
+    seg = prob.segments[s]
+    refs = _oracle_key_tiles(prob, inputs, s, g, kts)
+    for kt, (dK_ref, dV_ref) in zip(kts, refs):
+        rows = seg.k_off + np.arange(kt * 128, min(seg.k_len, kt * 128 + 128))
+        for name, x, r in (("dK", to_np(dk[rows, g]), dK_ref), ("dV", to_np(dv[rows, g]), dV_ref)):
+            assert np.linalg.norm(r) > 0, (prob.name, what, s, g, kt, name, "no attending row")
+            rel = np.linalg.norm(x - r) / np.linalg.norm(r)
+            assert rel <= BWD_REL_L2, (prob.name, what, s, g, kt, name, rel)
+
+
+def _partial_key_tiles(prob, s, h):
+    """Key tiles of segment s holding at least one 128x128 (query tile, key
+    tile) block that the oracle's mask for head h makes PARTIAL: some cells
+    attended, not all (a block cut by the segment's end counts as partial
+    when anything in it is attended, as the kernels treat it)."""
+    seg = prob.segments[s]
+    nk = -(-seg.k_len // 128)
+    part = np.zeros(nk, dtype=bool)
+    for r0 in range(0, seg.q_len, 128):
+        rows = np.arange(r0, min(seg.q_len, r0 + 128))
+        m = np.zeros((128, nk * 128), dtype=bool)
+        m[:rows.size, :seg.k_len] = oracle.segment_mask(prob.mask, s, seg, h, rows)
+        blk = m.reshape(128, nk, 128).transpose(1, 0, 2).reshape(nk, -1)
+        part |= blk.any(axis=1) & ~blk.all(axis=1)
+    return np.nonzero(part)[0]
+
+
+def _tiles_to_check(prob, s, h):
+    """The first, a middle and the last key tile of segment s, plus the
+    partial tile nearest three quarters of the way (if the mask has one)."""
+    nk = -(-prob.segments[s].k_len // 128)
+    kts = {0, nk // 2, nk - 1}
+    part = [kt for kt in _partial_key_tiles(prob, s, h) if kt not in kts]
+    if part:
+        kts.add(min(part, key=lambda kt: abs(kt - 3 * nk // 4)))
+    return sorted(kts)
+
+
+@pytest.mark.parametrize("kind", STATIC_KINDS)
+def test_static_sweep_8k_full_size(lca, kind):
+    """The benchmark's 8K static-mask sweep (GQA 64:8), each family in its own
+    full-size launch: O, LSE and dQ of one query head per KV group on the
+    first, middle and last 64 rows of three segments; dK/dV element-wise on
+    the first, a middle, the last and a partial key tile of the largest
+    segment (and, for document families, of a middle-sized and the smallest
+    document), in a different KV group per family; gradient sums everywhere."""
+    import torch
+
+    prob = config2(kind)
+    inputs, outputs = _run(lca, prob)
+    cpu_inputs = tuple(t.cpu() for t in inputs)
+    _check_rows(lca, prob, cpu_inputs, outputs, _one_head_per_group(prob))
+    g = STATIC_KINDS.index(kind) % prob.Hkv
+    G = prob.Hq // prob.Hkv
+    segs = _sample_segments(prob)
+    big = max(segs, key=lambda s: prob.segments[s].k_len)
+    _check_key_tiles(prob, cpu_inputs, outputs, big, g, _tiles_to_check(prob, big, g * G), "largest segment")
+    for s in segs:
+        if s != big:
+            nk = -(-prob.segments[s].k_len // 128)
+            _check_key_tiles(prob, cpu_inputs, outputs, s, g, sorted({0, nk - 1}), "other document")
+    _check_gradient_sums(prob, inputs, outputs)
+    torch.cuda.synchronize()
+
+
+def _check_document_key_tiles(prob, inputs, outputs, g, max_len=32768, budget=1 << 26):
+    """Interior key tiles of one document (key group) no longer than
+    `max_len`, element-wise against the oracle.  The oracle's cost is the
+    attending rows times the document's keys per head, kept near `budget`:
+    causal tiles move towards the document's end until at most
+    budget / k_len rows attend them.  For a shard batch the document is one
+    cut into several shards, and one tile lies just before its last shard, so
+    rows of two or more shards (segments sharing the key range) add up in it;
+    among such documents the cheapest is taken.  Otherwise the longest
+    document within the limit is taken (the smallest one if none is)."""
+    groups = {}
+    for s, seg in enumerate(prob.segments):
+        if seg.q_len > 0 and seg.k_len > 0:
+            groups.setdefault(seg.k_off, []).append(s)
+
+    def last(members):
+        return max(members, key=lambda i: prob.segments[i].k_len)
+
+    multi = [m for m in groups.values() if len(m) > 1 and prob.segments[last(m)].k_len <= max_len]
+    if multi:
+        members = min(multi, key=lambda m: prob.segments[last(m)].k_len * (prob.segments[last(m)].q_len + 256))
+    else:
+        fit = [m for m in groups.values() if prob.segments[last(m)].k_len <= max_len]
+        members = (max(fit, key=lambda m: prob.segments[last(m)].k_len) if fit
+                   else min(groups.values(), key=lambda m: prob.segments[last(m)].k_len))
+    s = last(members)
+    seg = prob.segments[s]
+    nk = -(-seg.k_len // 128)
+    max_rows = max(256, budget // seg.k_len)
+    kts = set()
+    for kt in (nk // 2, 2 * nk // 3):
+        while kt < nk - 1 and seg.k_len - kt * 128 > max_rows:
+            kt += 1
+        kts.add(kt)
+    if len(members) > 1:
+        first_row = seg.k_len - seg.q_len  # the last shard's first query position in its document
+        kts.add(max(0, first_row // 128 - 1))
+    _check_key_tiles(prob, inputs, outputs, s, g, sorted(kts), f"document of {seg.k_len} keys, {len(members)} segments")
+
+
 DENSE = [config3(S, heads, kind) for S in (8192, 49152) for heads in ("gqa", "mha") for kind in ("CAUSAL", "CAUSAL_DOC")]
 
 
@@ -138,6 +290,7 @@ def test_dense_sweep_full_size(lca, prob):
     _check_rows(lca, prob, inputs, outputs, _heads(prob))
     _check_last_key_tile(lca, prob, inputs, outputs, g=0)
     _check_last_key_tile(lca, prob, inputs, outputs, g=prob.Hkv - 1)
+    _check_document_key_tiles(prob, inputs, outputs, g=prob.Hkv // 2)
     _check_gradient_sums(prob, inputs, outputs)
 
 
@@ -163,6 +316,7 @@ def test_shard_batch_512k(lca):
     inputs, outputs = _run(lca, prob)
     _check_rows(lca, prob, inputs, outputs, _heads(prob))
     _check_last_key_tile(lca, prob, inputs, outputs, g=0)
+    _check_document_key_tiles(prob, inputs, outputs, g=3)
     _check_gradient_sums(prob, inputs, outputs)
     # same documents, one segment each, queries in document order
     from gen import MaskSpec, Problem, docs_to_segments

@@ -2,8 +2,9 @@
 callers that cannot allocate device memory — a process whose device-memory
 pool was reserved up front and may not grow, or code running where
 allocation is not allowed.  It must give the same result as the regular
-forward with a caller-provided workspace, call after call, and reject shapes
-whose workspace does not fit its fixed array before launching anything.
+forward with a caller-provided workspace, bit for bit, call after call,
+without allocating, and reject shapes whose workspace does not fit its fixed
+array before launching anything.
 
 This file is collected last on purpose: the static array keeps the previous
 call's contents, so these tests also show that a call clears what it needs."""
@@ -11,22 +12,19 @@ from __future__ import annotations
 
 import ctypes as C
 
-import numpy as np
 import pytest
 
+import oracle
 from gen import Segment, make_tensors
 from tests import cases
-from tests.gpu_util import check_fwd, to_np
+from tests.gpu_util import check_fwd
 
 pytestmark = pytest.mark.gpu
 
 
-def _static_fwd(lca, call, q, k, v):
+def _static_fwd(lca, call, q, k, v, o, lse):
     import torch
 
-    Tq, Hq, _ = q.shape
-    o = torch.empty_like(q)
-    lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
     code = lca.load().lca_attn_fwd_static_workspace(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                                     lse.data_ptr(), C.byref(call.shape), C.byref(call.mask), stream)
@@ -37,17 +35,35 @@ def _static_fwd(lca, call, q, k, v):
 
 @pytest.mark.parametrize("idx", [5, 12])  # causal documents; uniform 64-block sparse map
 def test_static_workspace_forward_matches_regular_forward(lca, idx):
+    """Both entry points run the same planner and kernels on the same inputs,
+    and the forward's result does not depend on which CTA takes which work
+    item, so O and LSE must be bit-identical to the regular forward's (and
+    within the parity bar of the oracle).  The second and third calls must
+    not change the memory PyTorch has allocated or the device's free memory:
+    the entry point allocates nothing once its first call on the device has
+    looked up the static array."""
     import torch
 
     prob = cases.gpu_small_all()[idx]
-    q, k, v, _ = (t.cuda() if t is not None else None for t in make_tensors(prob))
+    q_h, k_h, v_h, _ = make_tensors(prob)
+    q, k, v = q_h.cuda(), k_h.cuda(), v_h.cuda()
     call = lca.marshal(prob.Tq, prob.Tk, prob.Hq, prob.Hkv, prob.d, prob.segments, prob.mask, prob.scale)
     o_ref, lse_ref = lca.attn_fwd(q, k, v, prob.segments, prob.mask, prob.scale, call=call)
     torch.cuda.synchronize()
-    O_ref, L_ref = to_np(o_ref), to_np(lse_ref)
-    for _ in range(2):  # two calls in a row share the one static array
-        o, lse = _static_fwd(lca, call, q, k, v)
-        check_fwd(o, lse, O_ref, L_ref, what=f"static workspace {prob.name}")
+    O_ora, L_ora = oracle.attention_forward(prob, q_h, k_h, v_h)
+    o, lse = torch.empty_like(q), torch.empty((prob.Hq, prob.Tq), dtype=torch.float32, device=q.device)
+    _static_fwd(lca, call, q, k, v, o, lse)  # first call on this device: looks up the array
+    for _ in range(2):  # later calls share the one static array, which keeps the last call's contents
+        o.fill_(7.0)
+        lse.fill_(7.0)
+        torch.cuda.synchronize()
+        alloc0, free0 = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]
+        _static_fwd(lca, call, q, k, v, o, lse)
+        assert torch.cuda.memory_allocated() == alloc0
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert torch.equal(o, o_ref), f"static workspace {prob.name}: O differs from lca_attn_fwd"
+        assert torch.equal(lse, lse_ref), f"static workspace {prob.name}: LSE differs from lca_attn_fwd"
+        check_fwd(o, lse, O_ora, L_ora, what=f"static workspace {prob.name} vs oracle")
 
 
 def test_static_workspace_rejects_oversized_shape(lca):
