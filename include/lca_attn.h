@@ -310,6 +310,24 @@ LCA_API lca_status lca_probe_wait_timeout(void* workspace, size_t workspace_byte
  * entries, may be null).  Pass null to stop.  Process-wide, not thread-safe. */
 LCA_API lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t* phases);
 
+/* Profiling hook: per-CTA work and time of the attention kernels, the
+ * evidence for how evenly the cost-sorted persistent scheduler spreads work
+ * over the SMs.  With a non-null device buffer `buf` of at least
+ * LCA_CTA_PROFILE_BYTES (8-byte aligned), every later forward and backward
+ * call writes one record per CTA of each attention kernel it launches:
+ * kernel slot k (0 forward, 1 dK/dV, 2 dQ) starts at byte k * 1024 * 64, and
+ * CTA b's record at 64 * b within it, eight uint64 values:
+ *   start and end of the CTA (%globaltimer, ns), work items it ran, full and
+ *   partial tile units it ran (forward: 128-row query sub-tile x key tile;
+ *   dK/dV: 64-row query step; dQ: 128-row query tile x key tile), the grid
+ *   size, the SM it ran on, 0.
+ * A call clears its kernel's slot on its stream before the launch, so
+ * records of CTAs beyond the grid are zero.  Pass null to stop.
+ * LCA_ERR_INVALID_ARG for a short, misaligned or non-device buffer.
+ * Process-wide, not thread-safe. */
+#define LCA_CTA_PROFILE_BYTES (3u * 1024u * 64u)
+LCA_API lca_status lca_set_cta_profile(void* buf, size_t bytes);
+
 /* Text of the last CUDA failure seen by this library in the calling thread
  * (the failing call and the runtime's message), or "" if none. */
 LCA_API const char* lca_last_error_detail(void);

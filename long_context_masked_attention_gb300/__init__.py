@@ -4,6 +4,8 @@ from .binding import (  # noqa: F401
     EXPORTED,
     PHASES,
     KernelEvents,
+    CtaProfile,
+    PROFILE_KERNELS,
     launch_count,
     MASK_KINDS,
     LcaError,

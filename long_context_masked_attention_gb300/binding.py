@@ -26,7 +26,7 @@ STATUS = {0: "LCA_OK", 1: "LCA_ERR_INVALID_ARG", 2: "LCA_ERR_UNSUPPORTED", 3: "L
 EXPORTED = ("lca_workspace_size", "lca_attn_fwd", "lca_attn_bwd", "lca_mask_materialize", "lca_mask_tile_classes",
             "lca_mask_nnz", "lca_read_status", "lca_probe_wait_timeout", "lca_set_kernel_events", "lca_launch_count",
             "lca_last_error_detail", "lca_attn_fwd_static_workspace", "lca_status_string", "lca_version",
-            "lca_attn_merge", "lca_cad_plan", "lca_attn_fwd_dropout", "lca_attn_bwd_dropout")
+            "lca_attn_merge", "lca_cad_plan", "lca_attn_fwd_dropout", "lca_attn_bwd_dropout", "lca_set_cta_profile")
 PHASES = ("fwd_plan", "fwd", "d_prepass", "dkv_plan", "dkv", "dq_plan", "dq")
 
 
@@ -97,6 +97,7 @@ def load(path: str = LIB_PATH):
     lib.lca_read_status.argtypes = [vp, C.POINTER(C.c_int32), vp]
     lib.lca_probe_wait_timeout.argtypes = [vp, C.c_size_t, C.c_int32, vp]
     lib.lca_set_kernel_events.argtypes = [C.POINTER(C.c_void_p), C.c_int32, C.POINTER(C.c_int32)]
+    lib.lca_set_cta_profile.argtypes = [vp, C.c_size_t]
     lib.lca_launch_count.restype = C.c_uint64
     lib.lca_launch_count.argtypes = []
     lib.lca_attn_fwd_static_workspace.argtypes = [vp, vp, vp, vp, vp, C.POINTER(Shape_t), C.POINTER(MaskDesc_t), vp]
@@ -514,3 +515,37 @@ class KernelEvents:
 
 def launch_count() -> int:
     return int(load().lca_launch_count())
+
+
+CTA_PROFILE_BYTES = 3 * 1024 * 64
+PROFILE_KERNELS = ("fwd", "dkv", "dq")
+
+
+class CtaProfile:
+    """Per-CTA records of the attention kernels (lca_set_cta_profile): after a
+    call, records() gives for each kernel the rows (start_ns, end_ns, items,
+    full, partial, grid, sm) of the CTAs it launched."""
+
+    def __init__(self, device="cuda"):
+        import torch
+
+        self.buf = torch.zeros(CTA_PROFILE_BYTES // 8, dtype=torch.int64, device=device)
+
+    def start(self):
+        with _on_device(self.buf.device):
+            _check(load().lca_set_cta_profile(self.buf.data_ptr(), CTA_PROFILE_BYTES), "lca_set_cta_profile")
+
+    def stop(self):
+        _check(load().lca_set_cta_profile(None, 0), "lca_set_cta_profile")
+
+    def records(self):
+        """{kernel: int64 array [grid, 7]} for every kernel slot the last call
+        filled (call after a synchronize)."""
+        r = self.buf.view(3, 1024, 8).cpu().numpy()
+        out = {}
+        for k, name in enumerate(PROFILE_KERNELS):
+            grid = int(r[k, 0, 5])
+            if grid > 0:
+                out[name] = r[k, :grid, :7].copy()
+        return out
+

@@ -42,6 +42,22 @@ struct EventRing {
 };
 EventRing g_ring;
 
+// Per-CTA profile buffer (lca_set_cta_profile): kernel slot k at
+// k * kProfCtas records of 8 u64, or null when profiling is off.
+unsigned long long* g_prof = nullptr;
+
+// The profile records of kernel slot `k` for the launch about to be made on
+// `st` (cleared first, so that CTAs beyond the grid read as zero), or null.
+unsigned long long* prof_slot(int k, cudaStream_t st) {
+  if (!g_prof) return nullptr;
+  unsigned long long* p = g_prof + static_cast<size_t>(k) * kProfCtas * 8;
+  if (cudaMemsetAsync(p, 0, sizeof(unsigned long long) * kProfCtas * 8, st) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return p;
+}
+
 // Records the opening event of a phase; returns the pair index or -1.
 int phase_begin(int phase, cudaStream_t st) {
   if (!g_ring.events || g_ring.n_pairs == 0) return -1;
@@ -642,6 +658,17 @@ lca_status lca_set_kernel_events(void* const* events, int32_t n_events, int32_t*
   return LCA_OK;
 }
 
+lca_status lca_set_cta_profile(void* buf, size_t bytes) {
+  if (!buf) {
+    g_prof = nullptr;
+    return LCA_OK;
+  }
+  if (bytes < LCA_CTA_PROFILE_BYTES || (reinterpret_cast<uintptr_t>(buf) & 7u) != 0 || !device_input(buf))
+    return LCA_ERR_INVALID_ARG;
+  g_prof = static_cast<unsigned long long*>(buf);
+  return LCA_OK;
+}
+
 const char* lca_last_error_detail(void) { return g_err_detail; }
 
 uint64_t lca_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
@@ -737,6 +764,7 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     a.n_work = static_cast<int>(n_rows * wl.expand);
     a.o = o;
     a.lse = lse;
+    a.prof = prof_slot(0, c.st);
     ph = phase_begin(1, c.st);
     launch_fwd(tq, tk, tv, a, sms, c.st);
     phase_end(ph, c.st);
@@ -881,6 +909,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nlse2 = lse2;
     a.dk = dk;
     a.dv = dv;
+    a.prof = prof_slot(1, c.st);
     ph = phase_begin(4, c.st);
     launch_bwd_dkv(tq64, tk, tv, tdo64, a, sms, c.st);
     launch_dkv_reduce(a, c.st);
@@ -909,6 +938,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nD = D;
     a.nlse2 = lse2;
     a.dq = dq;
+    a.prof = prof_slot(2, c.st);
     ph = phase_begin(6, c.st);
     launch_bwd_dq(tq, tk, tv, tdo, a, sms, c.st);
     phase_end(ph, c.st);

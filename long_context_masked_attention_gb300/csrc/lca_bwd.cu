@@ -84,11 +84,14 @@ struct Item {
   long long ebase;
 };
 
+// `counts` (shared memory) receives the CTA's work items and its full and
+// partial key tiles, for the optional per-CTA profile.
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
-                                         Item* items) {
+                                         Item* items, uint32_t* counts) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  uint32_t n_items = 0, n_full = 0, n_part = 0;
   uint32_t tiles = 0;  // key tiles loaded so far
   uint32_t k_issued = 0, v_issued = 0;
   int q_issued = 0;
@@ -114,7 +117,13 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       }
       items[slot] = inf;
       mbar_arrive(&bar[B_ITFULL + slot]);
-      if (!inf.valid) return;
+      if (!inf.valid) {
+        counts[0] = n_items;
+        counts[1] = n_full;
+        counts[2] = n_part;
+        return;
+      }
+      ++n_items;
       const SegInfo sg = pv.segs[inf.seg];
       if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 111)) goto abort;
       mbar_arrive_expect_tx(&bar[B_QFULL], 2 * kTile128);
@@ -129,6 +138,8 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       for (int t = 0; t < inf.cnt; ++t, ++tiles) {
         const uint32_t e = e_next;
         if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
+        n_full += ((e >> 24) & 3u) == kTileFull;
+        n_part += ((e >> 24) & 3u) == kTilePartial;
         const int kt = static_cast<int>(e & 0xFFFFFFu);
         const int yk = sg.k_off + kt * kTile;
         const int kr = tiles % kKRing, vr = tiles % kVRing;
@@ -364,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
   Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
+  uint32_t* counts = reinterpret_cast<uint32_t*>(sm + kOffCtl + 768);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
@@ -376,6 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar[B_DSFULL + 1], 8);
     mbar_init(&bar[B_ITEMPTY], 9);
     mbar_init(&bar[B_ITEMPTY + 1], 9);
+    counts[0] = counts[1] = counts[2] = 0;
+    if (a.prof != nullptr) *reinterpret_cast<unsigned long long*>(counts + 4) = globaltimer_ns();
     fence_mbar_init();
   }
   tc_fence_before();
@@ -383,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   if (warp == 9) {
-    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
+    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items, counts);
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
@@ -395,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  if (a.prof != nullptr && threadIdx.x == 0) write_cta_record(a.prof, counts);
 }
 
 }  // namespace dq
@@ -455,13 +470,17 @@ __device__ __forceinline__ StepMeta* stat_meta(uint8_t* sm, int b) {
 // Steps of an item: for each query head of the KV head, each entry of its
 // list, each 64-row half of the 128-row query tile that lies inside the
 // segment and holds an attended cell.
+//
+// `counts` (shared memory) receives the CTA's work items and its full and
+// partial 64-row steps, for the optional per-CTA profile.
 template <bool kCols>
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, const CUtensorMap* tdo, uint8_t* sm, uint64_t* bar,
-                                         Item* items) {
+                                         Item* items, uint32_t* counts) {
   const PlanView& pv = a.pv;
   const int2* entries = static_cast<const int2*>(a.entries);
   const int lane = threadIdx.x & 31;
+  uint32_t n_items = 0, n_full = 0, n_part = 0;
   uint32_t steps = 0;
   int kv_issued = 0;
   int it = 0;
@@ -504,7 +523,15 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         items[slot] = inf;
         mbar_arrive(&bar[B_ITFULL + slot]);
       }
-      if (!inf.valid) return;
+      if (!inf.valid) {
+        if (lane == 0) {
+          counts[0] = n_items;
+          counts[1] = n_full;
+          counts[2] = n_part;
+        }
+        return;
+      }
+      ++n_items;
       const KeyGroup grp = pv.kgs[inf.kg];
       const int yk = grp.k_off + inf.kt * kTile;
       if (it >= 1 && !waitw(&bar[B_KVEMPTY], (it - 1) & 1, a, 211)) goto abort;
@@ -554,6 +581,8 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
                 continue;
               }
               ++us;
+              n_full += cls == kTileFull;
+              n_part += cls == kTilePartial;
               const int b = steps % kRing;
               const uint32_t reuse = steps / kRing;  // how many times ring slot b was filled before
               if (reuse >= 1 && !waitw(&bar[B_MEMPTY + b], (reuse - 1) & 1, a, 213)) goto abort;
@@ -858,6 +887,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
   Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
+  uint32_t* counts = reinterpret_cast<uint32_t*>(sm + kOffCtl + 768);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 8) {
     tmem_alloc(tmem_slot, 512);
@@ -872,6 +902,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bar[B_ITEMPTY], 9);
     mbar_init(&bar[B_ITEMPTY + 1], 9);
+    counts[0] = counts[1] = counts[2] = 0;
+    if (a.prof != nullptr) *reinterpret_cast<unsigned long long*>(counts + 4) = globaltimer_ns();
     fence_mbar_init();
   }
   tc_fence_before();
@@ -879,7 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   if (warp == 9) {
-    producer<kCols>(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items);
+    producer<kCols>(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items, counts);
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
@@ -891,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  if (a.prof != nullptr && threadIdx.x == 0) write_cta_record(a.prof, counts);
 }
 
 // One block per (sorted unit, KV head of the unit); blocks of units that were

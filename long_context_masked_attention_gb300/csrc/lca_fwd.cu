@@ -91,11 +91,14 @@ __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, const Attn
 }
 
 // ------------------------------------------------------------------ producer
+// `counts` (shared memory) receives the CTA's work items and its full and
+// partial (sub-tile, key tile) units, for the optional per-CTA profile.
 __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                                          const CUtensorMap* tv, uint8_t* sQ, uint8_t* sKV, uint64_t* bar,
-                                         Item* items) {
+                                         Item* items, uint32_t* counts) {
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
+  uint32_t n_items = 0, n_full = 0, n_part = 0;
   uint32_t kv_iter = 0;
   uint32_t issued = 0;  // K/V loads issued (ring index of the next one)
   int q_issued = 0;     // Q loads issued
@@ -121,7 +124,13 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       }
       items[slot] = inf;
       mbar_arrive(&bar[B_ITFULL + slot]);
-      if (!inf.valid) return;
+      if (!inf.valid) {
+        counts[0] = n_items;
+        counts[1] = n_full;
+        counts[2] = n_part;
+        return;
+      }
+      ++n_items;
 
       const SegInfo sg = pv.segs[inf.seg];
       if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 11)) goto abort;
@@ -141,6 +150,9 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       for (int t = 0; t < n; ++t) {
         const uint32_t e = e_next;
         if (t + 1 < n) e_next = entries[inf.ebase + t + 1];
+        const uint32_t c0 = (e >> 24) & 3u, c1 = (e >> 26) & 3u;
+        n_full += (c0 == kTileFull) + (c1 == kTileFull);
+        n_part += (c0 == kTilePartial) + (c1 == kTilePartial);
         const int yk = sg.k_off + static_cast<int>(e & 0xFFFFFFu) * kTile;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {  // K(t) then V(t)
@@ -494,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffCtl);
   Item* items = reinterpret_cast<Item*>(sm + kOffCtl + 512);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffCtl + 640);
+  uint32_t* counts = reinterpret_cast<uint32_t*>(sm + kOffCtl + 768);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -507,6 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bar[B_PFULL + x], 4);  // one arrival per softmax warp
       mbar_init(&bar[B_ITEMPTY + x], 9);
     }
+    counts[0] = counts[1] = counts[2] = 0;
+    if (a.prof != nullptr) *reinterpret_cast<unsigned long long*>(counts + 4) = globaltimer_ns();
     fence_mbar_init();
   }
   if (warp == 9 && lane == 0) {
@@ -520,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   if (warp == 9) {
-    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, sQ, sKV, bar, items);
+    if (lane == 0) producer(a, &tmQ, &tmK, &tmV, sQ, sKV, bar, items, counts);
   } else if (warp == 8) {
     mma_issuer(a, sQ, sKV, bar, items, tbase);
   } else {
@@ -532,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  if (a.prof != nullptr && threadIdx.x == 0) write_cta_record(a.prof, counts);
 }
 
 }  // namespace

@@ -11,6 +11,7 @@
 namespace lca {
 
 constexpr int kCostBuckets = 4096;  // histogram buckets of the cost sort
+constexpr int kProfCtas = 1024;     // CTA records per kernel in a profile buffer
 
 // Counts kernel launches made by this library (see lca_launch_count).
 void note_launches(int n);
@@ -107,6 +108,8 @@ struct AttnArgs {
   int n_units;
   int* status;
   unsigned long long wait_limit_ns;
+  // per-CTA profile records (kProfCtas x 8 u64), or null when profiling is off
+  unsigned long long* prof;
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   // dropout on P: threshold t (0 = off; keep probability (256 - t) / 256),

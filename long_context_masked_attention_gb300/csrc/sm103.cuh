@@ -22,6 +22,30 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
+// ---------------------------------------------------------------- CTA profile
+// One 64-byte record per CTA of an attention kernel, written when profiling
+// is switched on: start and end (%globaltimer, ns), the work items, full and
+// partial tile units the CTA ran, the grid size and the SM it ran on.
+// `counts` (shared memory) holds the three counts in words 0-2 and the start
+// time as a 64-bit value in words 4-5.
+__device__ __forceinline__ void write_cta_record(unsigned long long* prof, const uint32_t* counts) {
+  unsigned long long* r = prof + 8ull * blockIdx.x;
+  r[0] = *reinterpret_cast<const unsigned long long*>(counts + 4);
+  r[1] = globaltimer_ns();
+  r[2] = counts[0];
+  r[3] = counts[1];
+  r[4] = counts[2];
+  r[5] = gridDim.x;
+  r[6] = sm_id();
+  r[7] = 0;
+}
+
 // ---------------------------------------------------------------- status word
 // status[0]: first error code (0 = ok), status[1]: where it was raised.
 __device__ __forceinline__ void raise_status(int* status, int code, int where) {
