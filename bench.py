@@ -60,13 +60,17 @@ def peaks():
 
 def tensor_peak(pk, pk_src, clk):
     """The bf16 peak that matches the clocks sampled during the timed region:
-    the burst figure when the SM clock stayed at its maximum with no power
-    cap, else the sustained (power-capped) one."""
-    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
-    held = bool(clk.get("samples")) and sm and mx and sm >= 0.95 * mx and "sw_power_cap" not in clk.get("reasons", [])
+    the burst figure when the median SM clock stayed within 5% of its maximum
+    and the power cap was active in under a quarter of the samples, else the
+    sustained (power-capped) one."""
+    sm, mx, n = clk.get("sm_mhz"), clk.get("sm_max_mhz"), clk.get("samples") or 0
+    capped = clk.get("reason_samples", {}).get("sw_power_cap", 0)
+    held = n > 0 and sm and mx and sm >= 0.95 * mx and capped < 0.25 * n
     if held:
-        return pk["bf16_tflops"], f"{pk_src} bf16 burst (SM clock held at its maximum, no power cap seen)"
-    return pk["bf16_tflops_sustained"], f"{pk_src} bf16 sustained (power cap seen or clock below maximum)"
+        return pk["bf16_tflops"], (f"{pk_src} bf16 burst (median SM clock at its maximum; power cap in {capped} of "
+                                   f"{n} samples)")
+    return pk["bf16_tflops_sustained"], (f"{pk_src} bf16 sustained (power cap in {capped} of {n} samples, or clock "
+                                         f"below its maximum)")
 
 
 WORKLOADS = {
@@ -136,6 +140,78 @@ def time_problem(lca, p, ws, flush, steps, warmup, tensors=None, dropout=None):
             "tflops": (fl_f + fl_b) / ((f_ms + b_ms) * 1e-3) / 1e12}
 
 
+# ------------------------------------------------------------------ spec targets
+def target_problems():
+    """Dense GQA 64:8 CAUSAL and FULL at 8K, 16K, 32K and 48K (48K tokens per
+    problem: floor(49152 / S) sequences of S tokens) and MHA 64:64 CAUSAL at
+    8K, for the ">= 60% of peak for dense causal/full at 8K-48K" reading."""
+    from gen import MaskSpec, Problem, config3
+
+    out = []
+    for S in (8192, 16384, 32768, 49152):
+        c = config3(S, "gqa", "CAUSAL")
+        out.append(c)
+        out.append(Problem(c.name.replace("causal", "full"), c.Tq, c.Tk, c.Hq, c.Hkv, c.d, c.segments,
+                           MaskSpec("FULL"), c.seed))
+    out.append(config3(8192, "mha", "CAUSAL"))
+    return out
+
+
+def run_targets(lca, ws_dev, flush, pk, pk_src, gpu_index, steps=3, warmup=2):
+    """Forward, backward and combined effective TFLOP/s of the target
+    problems, each as a fraction of the bf16 peak matching the clocks sampled
+    while they ran (a few steps each, L2 flushed before every step)."""
+    import torch
+
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    rows = {}
+    for p in target_problems():
+        call = lca.marshal(p.Tq, p.Tk, p.Hq, p.Hkv, p.d, p.segments, p.mask, p.scale)
+        ws = torch.empty(lca.workspace_size(call, True), dtype=torch.uint8, device=ws_dev)
+        rows[p.name] = time_problem(lca, p, ws, flush, steps, warmup)
+        del ws
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    peak, src = tensor_peak(pk, pk_src, clk)
+    for r in rows.values():
+        r["frac_of_peak"] = r["tflops"] / peak
+        r["frac_of_sustained"] = r["tflops"] / pk["bf16_tflops_sustained"]
+    return {"peak_tflops": peak, "peak_source": src, "clocks": clk, "steps": steps, "warmup": warmup,
+            "problems": rows}
+
+
+def run_balance(lca, probs, calls, ws, tensors):
+    """Per-CTA balance of the attention kernels: one profiled forward and
+    backward per problem (outside every timed region); for each kernel the
+    slowest CTA's busy time over the mean (max_over_mean) and the share of
+    CTA-time spent idle before the kernel's last CTA finished (idle)."""
+    import torch
+
+    prof = lca.CtaProfile(ws.device)
+    q, k, v, do = tensors
+    out = {}
+    for p, c in zip(probs, calls):
+        prof.start()
+        try:
+            o, lse = lca.attn_fwd(q, k, v, p.segments, p.mask, p.scale, workspace=ws, call=c)
+            torch.cuda.synchronize()
+            rec = {"fwd": prof.records()["fwd"]}
+            lca.attn_bwd(do, q, k, v, o, lse, p.segments, p.mask, p.scale, workspace=ws, call=c)
+            torch.cuda.synchronize()
+            rec.update({kk: vv for kk, vv in prof.records().items() if kk != "fwd"})
+        finally:
+            prof.stop()
+        row = {}
+        for name, r in rec.items():
+            busy = (r[:, 1] - r[:, 0]).astype(float)
+            span = float(r[:, 1].max() - r[:, 0].min())
+            row[name] = {"max_over_mean": float(busy.max() / busy.mean()), "idle": float(1.0 - busy.mean() / span),
+                         "ctas": int(r.shape[0])}
+        out[p.mask.kind] = row
+    return out
+
+
 # ------------------------------------------------------------------ measured traffic
 TRAFFIC_PROFILES = {"dkv": "profiles/dkv_kernel_traffic_sweep8k_gqa64x8.md"}
 
@@ -171,15 +247,17 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 25):
         self.proc = None
         self.gpu = gpu_index
+        self.interval_ms = interval_ms
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
-                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms",
+                 str(self.interval_ms), "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
         except OSError:
             self.proc = None
 
@@ -192,22 +270,28 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(out: str):
+    """Median SM clock, maximum clock, the throttle reasons seen and, per
+    reason, the number of samples it was active in."""
+    sm, mx, counts = [], [], {}
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                counts[n] = counts.get(n, 0) + 1
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": sorted(counts), "samples": len(sm), "reason_samples": counts}
 
 
 # ------------------------------------------------------------------ distributed helpers
@@ -509,6 +593,14 @@ def run_ours(args):
     per_mask = {}
     for p in probs:
         per_mask[p.mask.kind] = time_problem(lca, p, ws, flush, args.steps, 1, tensors=(q, k, v, do))
+    causal = per_mask.get("CAUSAL", {}).get("tflops")
+    if causal:
+        for r in per_mask.values():
+            r["rel_to_causal"] = r["tflops"] / causal
+    balance = run_balance(lca, probs, calls, ws, (q, k, v, do)) if not args.no_balance else None
+    targets = None
+    if not args.no_targets and args.only is None:
+        targets = run_targets(lca, dev, flush, *peaks(), clocks.gpu)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -518,7 +610,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_peak": 100.0 * value / peak, "peak_tflops": peak, "peak_source": peak_src,
         "roofline": roofline, "phase_ms_per_step": phase_ms, "gpu_launches": launches,
-        "clocks": clk, "e2e": e2e, "per_mask": per_mask,
+        "clocks": clk, "e2e": e2e, "per_mask": per_mask, "balance": balance, "targets": targets,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         try:
@@ -593,6 +685,8 @@ def main(argv=None):
                     help="end-to-end leg: outputs copied out (default), or gradients stored by the kernels into "
                          "mapped pinned host memory (slower on a GB300: the stores stall the backward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-targets", action="store_true", help="skip the dense 8K-48K target problems")
+    ap.add_argument("--no-balance", action="store_true", help="skip the per-CTA balance profile")
     ap.add_argument("--only", default=None, help="comma-separated mask kinds or problem names (partial runs)")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="sweep8k")
     ap.add_argument("--_oracle_sample", default=None, help=argparse.SUPPRESS)

@@ -75,7 +75,7 @@ void phase_end(int p, cudaStream_t st) {
 }
 
 constexpr size_t kAlign = 256;
-constexpr size_t kMaxPartialSlots = 256;  // 32 MiB of f32 dK/dV partial sums at most
+constexpr size_t kMaxPartialSlots = 512;  // 64 MiB of f32 dK/dV partial sums at most
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
@@ -109,10 +109,10 @@ struct Layout {
          b_parts = 0, b_qbb = 0, b_kbb = 0;
   size_t keep = 0, keep_bytes = 0, qb_of = 0, kb_of = 0;
   size_t tcls = 0;
-  size_t f_cnt = 0, f_order = 0, f_ent = 0;
-  size_t D = 0, lse2 = 0, q_cnt = 0, q_order = 0, q_ent = 0, k_ucnt = 0, k_order = 0, k_lcnt = 0, k_lsteps = 0,
-         k_ent = 0;
-  size_t k_usteps = 0, k_nchunk = 0, k_istart = 0, k_sstart = 0, k_nwork = 0, k_part = 0;
+  size_t f_cnt = 0, f_key = 0, f_order = 0, f_ent = 0;
+  size_t D = 0, lse2 = 0, q_cnt = 0, q_key = 0, q_order = 0, q_ent = 0, k_ucost = 0, k_key = 0, k_order = 0,
+         k_lcnt = 0, k_lsteps = 0, k_ent = 0;
+  size_t k_usteps = 0, k_nchunk = 0, k_istart = 0, k_sstart = 0, k_nwork = 0, k_part = 0, k_runfirst = 0, k_runof = 0;
   int k_max_slots = 0;
   size_t total = 0;
 };
@@ -351,6 +351,7 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
   L.tcls = take(std::max<size_t>(1, H * P.dq_per_hm));
   if (fwd) {
     L.f_cnt = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
+    L.f_key = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
     L.f_order = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
     L.f_ent = take(sizeof(uint32_t) * std::max<size_t>(1, H * P.fwd_per_hm));
   }
@@ -359,9 +360,11 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     L.D = take(sizeof(float) * std::max<size_t>(1, static_cast<size_t>(P.Hq) * P.Tq));
     L.lse2 = take(sizeof(float) * std::max<size_t>(1, static_cast<size_t>(P.Hq) * P.Tq));
     L.q_cnt = take(sizeof(int) * std::max<size_t>(1, H * P.R128));
+    L.q_key = take(sizeof(int) * std::max<size_t>(1, H * P.R128));
     L.q_order = take(sizeof(int) * std::max<size_t>(1, H * P.R128));
     L.q_ent = take(sizeof(uint32_t) * std::max<size_t>(1, H * P.dq_per_hm));
-    L.k_ucnt = take(sizeof(int) * std::max<size_t>(1, hkv_m * P.RK));
+    L.k_ucost = take(sizeof(int) * std::max<size_t>(1, hkv_m * P.RK));
+    L.k_key = take(sizeof(int) * std::max<size_t>(1, hkv_m * P.RK));
     L.k_order = take(sizeof(int) * std::max<size_t>(1, hkv_m * P.RK));
     L.k_lcnt = take(sizeof(int) * std::max<size_t>(1, H * P.RK));
     L.k_lsteps = take(sizeof(int) * std::max<size_t>(1, H * P.RK));
@@ -371,9 +374,11 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     L.k_nchunk = take(sizeof(int) * n_units);
     L.k_istart = take(sizeof(int) * (n_units + 1));
     L.k_sstart = take(sizeof(int) * n_units);
-    L.k_nwork = take(sizeof(int));
+    L.k_nwork = take(2 * sizeof(int));
+    L.k_runfirst = take(sizeof(int) * n_units);
+    L.k_runof = take(sizeof(int) * n_units);
     // partial-sum slots for chunks of split dK/dV units: [slot][dV, dK][128][128] f32
-    L.k_max_slots = static_cast<int>(std::min<size_t>(kMaxPartialSlots, n_units * (P.Hkv / hkv_m)));
+    L.k_max_slots = static_cast<int>(std::min<size_t>(kMaxPartialSlots, 2 * n_units * (P.Hkv / hkv_m)));
     L.k_part = take(sizeof(float) * 2 * kTile * kHeadDim * static_cast<size_t>(L.k_max_slots));
   }
   L.total = o;
@@ -743,6 +748,7 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
   if (n_rows > 0) {
     WorkList wl{};
     wl.cnt = reinterpret_cast<int*>(c.ws + c.L.f_cnt);
+    wl.key = reinterpret_cast<int*>(c.ws + c.L.f_key);
     wl.order = reinterpret_cast<int*>(c.ws + c.L.f_order);
     wl.entries = c.ws + c.L.f_ent;
     wl.hist = reinterpret_cast<uint32_t*>(c.ws + c.L.hist);
@@ -868,7 +874,8 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
   phase_end(ph, c.st);
   if (k_units > 0) {
     WorkList wl{};
-    wl.cnt = reinterpret_cast<int*>(c.ws + c.L.k_ucnt);
+    wl.cnt = reinterpret_cast<int*>(c.ws + c.L.k_ucost);
+    wl.key = reinterpret_cast<int*>(c.ws + c.L.k_key);
     wl.order = reinterpret_cast<int*>(c.ws + c.L.k_order);
     wl.entries = c.ws + c.L.k_ent;
     wl.hist = hist + kCostBuckets;
@@ -884,6 +891,8 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     sp.split_start = reinterpret_cast<int*>(c.ws + c.L.k_sstart);
     sp.n_work = reinterpret_cast<int*>(c.ws + c.L.k_nwork);
     sp.max_slots = c.L.k_max_slots;
+    sp.run_first = reinterpret_cast<int*>(c.ws + c.L.k_runfirst);
+    sp.run_of = reinterpret_cast<int*>(c.ws + c.L.k_runof);
     ph = phase_begin(3, c.st);
     launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, c.st);
     launch_sort(wl, c.st);
@@ -903,6 +912,8 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nchunk = sp.nchunk;
     a.usteps = usteps;
     a.n_work_dev = sp.n_work;
+    a.run_first = sp.run_first;
+    a.run_of = sp.run_of;
     a.partials = reinterpret_cast<float*>(c.ws + c.L.k_part);
     a.n_units = static_cast<int>(k_units);
     a.nD = D;
@@ -918,6 +929,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
   if (q_rows > 0) {
     WorkList wl{};
     wl.cnt = reinterpret_cast<int*>(c.ws + c.L.q_cnt);
+    wl.key = reinterpret_cast<int*>(c.ws + c.L.q_key);
     wl.order = reinterpret_cast<int*>(c.ws + c.L.q_order);
     wl.entries = c.ws + c.L.q_ent;
     wl.hist = hist + 2 * kCostBuckets;

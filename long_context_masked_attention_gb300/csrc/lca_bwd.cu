@@ -484,7 +484,8 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
   uint32_t steps = 0;
   int kv_issued = 0;
   int it = 0;
-  const int n_work = *a.n_work_dev;
+  const int n_work = a.n_work_dev[0];
+  const int n_runs = a.n_work_dev[1];
   for (;; ++it) {
     const int slot = it & 1;
     if (it >= 2 && !waitw(&bar[B_ITEMPTY + slot], ((it >> 1) - 1) & 1, a, 210)) goto abort;
@@ -497,22 +498,28 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       if (w < n_work) {
         // sorted unit i holding item w; its items are chunk-major, then KV head, so the
         // cost order (longest first) holds across heads and chunks
-        int lo = 0, hi = a.n_units;
+        int lo = 0, hi = n_runs;
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
           if (a.item_start[mid] <= w) lo = mid; else hi = mid;
         }
-        const int unit = a.order[lo];
+        // run `lo` holds item w; inside a run items go chunk, KV head, unit
+        const int first = a.run_first[lo];
+        const int n_r = ((lo + 1 < n_runs) ? a.run_first[lo + 1] : a.n_units) - first;
         const int local = w - a.item_start[lo];
+        const int per_chunk = n_r * a.expand;
+        const int c = local / per_chunk;
+        const int rem = local % per_chunk;
+        const int e = rem / n_r;
+        const int unit = a.order[first + rem % n_r];
         const int P = a.nchunk[unit];
-        const int c = local / a.expand;
         const int gm = unit / pv.RK, rk = unit % pv.RK;
         const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
         inf.valid = 1;
         inf.kg = kg;
         inf.kt = rk - pv.kt_start[kg];
         inf.rk = rk;
-        inf.g = (pv.hm_count == 1) ? (local % a.expand) : gm;
+        inf.g = (pv.hm_count == 1) ? e : gm;
         inf.unit_hm = 0;
         const long long S = a.usteps[unit];
         inf.begin = static_cast<int>(S * c / P);
@@ -548,15 +555,31 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       for (int l = 0; l < pv.G && us < us_end; ++l) {
         const int h = inf.g * pv.G + l;
         const int hm = (pv.hm_count == 1) ? 0 : h;
+        // a chunk starting further on skips whole query-head lists, then whole
+        // batches of 32 entries, by their step counts
+        const int list_steps = a.list_steps[hm * pv.RK + inf.rk];
+        if (us + list_steps <= inf.begin) {
+          us += list_steps;
+          continue;
+        }
         const int n_in_list = a.list_cnt[hm * pv.RK + inf.rk];
         const long long ebase = hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(inf.kt) * grp.pairs;
         for (int e0 = 0; e0 < n_in_list && us < us_end; e0 += 32) {
           // lane-parallel fetch of up to 32 entries and their segments
           int2 en = make_int2(0, 0);
           SegInfo sgl{};
+          int my_steps = 0;
           if (e0 + lane < n_in_list) {
             en = entries[ebase + e0 + lane];
             sgl = pv.segs[en.x];
+            const int qt = en.y & 0xFFFFFF;
+            const uint32_t sk = static_cast<uint32_t>(en.y >> 26) & 3u;
+            my_steps = ((sk & 1u) ? 0 : 1) + ((qt * kTile + 64 < sgl.q_len && !(sk & 2u)) ? 1 : 0);
+          }
+          const int batch_steps = __reduce_add_sync(0xFFFFFFFFu, my_steps);
+          if (us + batch_steps <= inf.begin) {
+            us += batch_steps;
+            continue;
           }
           const int batch = min(32, n_in_list - e0);
           for (int t = 0; t < batch && us < us_end; ++t) {
@@ -933,6 +956,10 @@ __global__ void __launch_bounds__(256) reduce_kernel(const AttnArgs a) {
   const int unit = a.order[i];
   const int P = a.nchunk[unit];
   if (P <= 1) return;
+  const int r = a.run_of[i];
+  const int first = a.run_first[r];
+  const int n_runs = a.n_work_dev[1];
+  const int n_r = ((r + 1 < n_runs) ? a.run_first[r + 1] : a.n_units) - first;
   const PlanView& pv = a.pv;
   const int gm = unit / pv.RK, rk = unit % pv.RK;
   const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
@@ -947,7 +974,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(const AttnArgs a) {
     if (jg >= grp.k_len) continue;
     float4 sv = make_float4(0.f, 0.f, 0.f, 0.f), sk = sv;
     for (int c = 0; c < P; ++c) {
-      const float* base = a.partials + static_cast<size_t>(a.split_start[i] + c * a.expand + gi) * (2 * kTile * kHeadDim);
+      const float* base = a.partials + static_cast<size_t>(a.split_start[r] + (c * a.expand + gi) * n_r + (i - first)) *
+                                           (2 * kTile * kHeadDim);
       const float4 v = *reinterpret_cast<const float4*>(base + j * kHeadDim + d4);
       const float4 k = *reinterpret_cast<const float4*>(base + kTile * kHeadDim + j * kHeadDim + d4);
       sv.x += v.x; sv.y += v.y; sv.z += v.z; sv.w += v.w;

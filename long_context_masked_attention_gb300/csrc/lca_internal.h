@@ -13,6 +13,18 @@ namespace lca {
 constexpr int kCostBuckets = 4096;  // histogram buckets of the cost sort
 constexpr int kProfCtas = 1024;     // CTA records per kernel in a profile buffer
 
+// Cost of a FULL and a PARTIAL tile unit in the longest-first schedules
+// (forward: 128-row sub-tile x key tile; dQ: 128x128 tile; dK/dV: 64-row
+// query step), in units of a quarter of a full unit; how they were measured
+// is described with the planner in lca_plan.cu.
+struct CostWeights {
+  int full, partial;
+};
+constexpr CostWeights kCostFwd{4, 10}, kCostDq{4, 5}, kCostDkv{4, 6};
+// A dK/dV chunk is at least this many 64-row steps long (a chunk pays a K/V
+// load and an epilogue, worth about ten steps).
+constexpr int kMinChunkSteps = 64;
+
 // Counts kernel launches made by this library (see lca_launch_count).
 void note_launches(int n);
 
@@ -37,7 +49,8 @@ struct PlanView {
 
 // Work lists produced by the planner for one kernel.
 struct WorkList {
-  int* cnt;           // entries per list row
+  int* cnt;           // entries per list row (dK/dV: weighted step cost per unit)
+  int* key;           // cost bucket per row or unit (the sort key)
   int* order;         // rows (or units) sorted by descending cost
   void* entries;      // uint32 (query-major) or int2 (key-major) entries
   uint32_t* hist;     // [kCostBuckets]
@@ -57,11 +70,15 @@ void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl,
 void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, int* list_cnt, int* list_steps,
                      int* usteps, cudaStream_t st);
 // Chunk counts, item and partial-slot prefixes over the cost-sorted units.
+// Chunk counts per unit; runs of sorted units (same cost bucket and chunk
+// count) with their item and partial-slot prefixes.
 struct DkvSplit {
-  int* nchunk;
-  int* item_start;
-  int* split_start;
-  int* n_work;
+  int* nchunk;       // per unit: chunks of each of its items (1 = whole)
+  int* item_start;   // per run: first work item (n_runs + 1 entries)
+  int* split_start;  // per run: first partial slot
+  int* n_work;       // [0] work items, [1] runs
+  int* run_first;    // per run: first sorted unit
+  int* run_of;       // per sorted unit: its run
   int max_slots;
 };
 void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st);
@@ -97,13 +114,16 @@ struct AttnArgs {
   int* counter;
   int n_work;
   int expand;
-  // dK/dV: units longer than a share of the per-SM load are cut into chunks of
-  // 64-row steps; a chunk writes f32 partial dV, dK that a reduction sums.
-  const int* item_start;   // [n_units + 1] first work item of each sorted unit
-  const int* split_start;  // [n_units] first partial slot of each sorted unit
+  // dK/dV: units far longer than a share of the per-SM load, and the last
+  // units of the cost order, are cut into chunks of 64-row steps; a chunk
+  // writes f32 partial dV, dK that a reduction sums.
+  const int* item_start;   // [n_runs + 1] first work item of each run of sorted units
+  const int* split_start;  // [n_runs] first partial slot of each run
   const int* nchunk;       // [unit] chunks of each of the unit's items (1 = whole)
   const int* usteps;       // [unit] 64-row steps of each of the unit's items
-  const int* n_work_dev;   // work items, written on the device by the split pass
+  const int* n_work_dev;   // [0] work items, [1] runs, written on the device by the split pass
+  const int* run_first;    // [n_runs] first sorted unit of each run
+  const int* run_of;       // [n_units] run of each sorted unit
   float* partials;         // [slot][dV, dK][128 rows][128] f32
   int n_units;
   int* status;

@@ -99,13 +99,44 @@ void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st) {
   classify_tiles_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(pv, tcls, total);
 }
 
+// ---------------------------------------------------------------- cost model
+// The schedulers hand out work longest first, by a cost that counts a
+// kernel's tile units by class: cost = n_full * w_full + n_partial * w_partial
+// (forward: 128-row sub-tile x key tile; dQ: 128-row query tile x key tile;
+// dK/dV: 64-row query step).  A PARTIAL unit costs more than a FULL one
+// because its mask is evaluated and applied element by element and, in the
+// forward, because its softmax chain is on the critical path.  The weights
+// are the ratios of the per-unit times fitted (least squares, time = a*full
+// + b*partial + c*items) over every CTA's %globaltimer busy time and unit
+// counts on the twelve 8K static masks (GQA 64:8): forward b/a = 2.6, dK/dV
+// 1.5, dQ 1.2 (the weights, kCostFwd, kCostDq and kCostDkv, are in
+// lca_internal.h, where the host sizes the dK/dV shares with them).
+
+__device__ __forceinline__ int unit_cost(uint32_t cls, CostWeights w) {
+  return cls == kTileFull ? w.full : (cls == kTilePartial ? w.partial : 0);
+}
+
+// Histogram bucket of a cost for the counting sort: exact below 1024, then
+// coarser in three steps (4, 32 and 256 cost units per bucket, a relative
+// resolution better than 0.7%), capped at the last bucket (cost 300032).
+__device__ __forceinline__ int cost_bucket(long long c) {
+  long long b;
+  if (c < 1024) b = c;
+  else if (c < 5120) b = 1024 + (c - 1024) / 4;
+  else if (c < 37888) b = 2048 + (c - 5120) / 32;
+  else b = 3072 + (c - 37888) / 256;
+  return static_cast<int>(b < kCostBuckets - 1 ? b : kCostBuckets - 1);
+}
+
 // ---------------------------------------------------------------- query-major lists
 // One warp per list row (map head, segment, query block of SUB*128 rows); the
 // warp takes 32 key tiles at a time and places the non-empty ones with a ballot.
 // Entry = key tile index | class of sub-tile 0 << 24 | class of sub-tile 1 << 26.
+// cnt = entries of the row, key = its cost bucket.
 template <int SUB>
 __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ cnt,
-                                   uint32_t* __restrict__ entries, uint32_t* __restrict__ hist) {
+                                   int* __restrict__ key, uint32_t* __restrict__ entries,
+                                   uint32_t* __restrict__ hist, CostWeights w) {
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int R = (SUB == 2) ? pv.R256 : pv.R128;
@@ -121,7 +152,7 @@ __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls
   uint32_t* out = entries + hm * per_hm + off + static_cast<long long>(qb) * sg.nk;
   const uint8_t* cls0 = tcls + hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(qb * SUB) * sg.nk;
   const bool has1 = (SUB == 2) && (qb * SUB + 1 < nq);
-  int n = 0;
+  int n = 0, cost = 0;
   for (int k0 = 0; k0 < sg.nk; k0 += 32) {
     const int kt = k0 + lane;
     uint32_t c0 = 0, c1 = 0;
@@ -132,10 +163,13 @@ __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls
     const uint32_t keep = __ballot_sync(0xFFFFFFFFu, (c0 | c1) != 0);
     if ((c0 | c1) != 0) out[n + __popc(keep & ((1u << lane) - 1u))] = static_cast<uint32_t>(kt) | (c0 << 24) | (c1 << 26);
     n += __popc(keep);
+    cost += __reduce_add_sync(0xFFFFFFFFu, unit_cost(c0, w) + unit_cost(c1, w));
   }
   if (lane == 0) {
     cnt[row] = n;
-    atomicAdd(hist + min(n, kCostBuckets - 1), 1u);
+    const int b = cost_bucket(cost);
+    key[row] = b;
+    atomicAdd(hist + b, 1u);
   }
 }
 
@@ -143,16 +177,16 @@ void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl
   const int rows = pv.hm_count * pv.R256;
   if (rows == 0) return;
   note_launches(1);
-  plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, static_cast<uint32_t*>(wl.entries),
-                                                        wl.hist);
+  plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, wl.key,
+                                                        static_cast<uint32_t*>(wl.entries), wl.hist, kCostFwd);
 }
 
 void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st) {
   const int rows = pv.hm_count * pv.R128;
   if (rows == 0) return;
   note_launches(1);
-  plan_q_rows_kernel<1><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, static_cast<uint32_t*>(wl.entries),
-                                                        wl.hist);
+  plan_q_rows_kernel<1><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, wl.key,
+                                                        static_cast<uint32_t*>(wl.entries), wl.hist, kCostDq);
 }
 
 // ---------------------------------------------------------------- key-major lists
@@ -161,10 +195,12 @@ void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl,
 // head of the KV head.  Entry = {segment, query tile | class byte << 24}; the
 // class byte keeps its half-empty flags, and a unit counts one step per
 // 64-row half that lies inside the segment and is not flagged empty.
-__global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ ucnt,
-                                     int* __restrict__ list_cnt, int* __restrict__ list_steps,
-                                     int* __restrict__ usteps, int2* __restrict__ entries,
-                                     uint32_t* __restrict__ hist, int n_units) {
+// ucost = the unit's weighted step cost (all G query heads), key = its bucket.
+__global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ ucost,
+                                     int* __restrict__ key, int* __restrict__ list_cnt,
+                                     int* __restrict__ list_steps, int* __restrict__ usteps,
+                                     int2* __restrict__ entries, uint32_t* __restrict__ hist, int n_units,
+                                     CostWeights w) {
   const int unit = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (unit >= n_units) return;
@@ -173,7 +209,7 @@ __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tc
   const KeyGroup grp = pv.kgs[kg];
   const int kt = rk - pv.kt_start[kg];
   const int nlists = (pv.hm_count == 1) ? 1 : pv.G;
-  int cost = 0, unit_steps = 0;
+  int cost = 0, unit_steps = 0;  // weighted step cost and steps over the unit's lists
   for (int l = 0; l < nlists; ++l) {
     const int hm = (pv.hm_count == 1) ? 0 : gm * pv.G + l;
     int2* out = entries + hm * pv.dkv_per_hm + grp.entry_off + static_cast<long long>(kt) * grp.pairs;
@@ -195,20 +231,23 @@ __global__ void plan_kv_units_kernel(PlanView pv, const uint8_t* __restrict__ tc
         }
         n += __popc(keep);
         steps += __reduce_add_sync(0xFFFFFFFFu, my_steps);
+        cost += __reduce_add_sync(0xFFFFFFFFu, my_steps * unit_cost(c & 3u, w));
       }
     }
     if (lane == 0) {
       list_cnt[hm * pv.RK + rk] = n;
       list_steps[hm * pv.RK + rk] = steps;
     }
-    cost += n;
     unit_steps += steps;
   }
   if (lane == 0) {
-    ucnt[unit] = cost;
     // one work item covers all G query heads of a KV head; a shared map is one list used G times
-    usteps[unit] = (pv.hm_count == 1) ? pv.G * unit_steps : unit_steps;
-    atomicAdd(hist + min(cost, kCostBuckets - 1), 1u);
+    const int mult = (pv.hm_count == 1) ? pv.G : 1;
+    usteps[unit] = mult * unit_steps;
+    ucost[unit] = mult * cost;
+    const int b = cost_bucket(static_cast<long long>(mult) * cost);
+    key[unit] = b;
+    atomicAdd(hist + b, 1u);
   }
 }
 
@@ -217,18 +256,34 @@ void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl
   const int n_units = wl.n_sorted;
   if (n_units == 0) return;
   note_launches(1);
-  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, list_cnt, list_steps, usteps,
-                                                          static_cast<int2*>(wl.entries), wl.hist, n_units);
+  plan_kv_units_kernel<<<(n_units + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, wl.key, list_cnt, list_steps, usteps,
+                                                          static_cast<int2*>(wl.entries), wl.hist, n_units,
+                                                          kCostDkv);
 }
 
 // ---------------------------------------------------------------- dK/dV split
-// One block.  A unit whose items are longer than 3/4 of the average per-SM
-// load (and than kMinChunkSteps) is cut into equal chunks of steps, so that a
-// few very long key tiles (keys every query attends, as with global tokens)
-// do not set the kernel's length.  Chunks of one item write partial sums to
-// their own slots; if the slots would run out, chunks grow until they fit.
-constexpr int kMinChunkSteps = 64;
-
+// One block.  The persistent CTAs claim dK/dV work items in cost order, so a
+// CTA that finishes early takes the next item; what is left unbalanced is
+// the end.  Two cuts keep it short:
+//  * a unit whose items cost more than 3/4 of the average per-SM load (and
+//    are longer than two minimum chunks) is cut into chunks of about that
+//    cost, so that a few very long key tiles (keys every query attends, as
+//    with global tokens) do not set the kernel's length;
+//  * the units holding the last num_sms (unit, KV head) items of the cost
+//    order are cut in two, so that the last round of claims is made of
+//    half-size items: with equal units (every key tile of a FULL or sliding
+//    mask: 512 units on 152 SMs) whole units leave 56 SMs a fourth unit
+//    while the other 96 idle.
+// Chunks split a unit's steps evenly and write partial sums to their own
+// slots; if the slots would run out, the tail cut covers fewer units, then
+// long-unit chunks grow, until they fit.
+//
+// Work items are then numbered by runs: maximal stretches of the sorted
+// units with the same cost bucket and chunk count.  Inside a run the items
+// go chunk by chunk, then KV head by KV head, then unit by unit, so that the
+// CTAs claiming consecutive items work on the same KV head's query rows at
+// the same time (they share Q and dO tiles in L2) while the order across
+// runs stays longest first.
 __device__ __forceinline__ long long block_sum_ll(long long v, long long* red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
@@ -262,66 +317,109 @@ __device__ __forceinline__ int block_scan_excl(int v, int* red, int& total) {
   return before + incl - v;
 }
 
-__global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__ order, const int* __restrict__ usteps,
-                                                         int n_units, int expand, int num_sms, int max_slots,
-                                                         int* __restrict__ nchunk, int* __restrict__ item_start,
-                                                         int* __restrict__ split_start, int* __restrict__ n_work) {
+// Chunks of the unit at sorted position i: the long-unit cut by `target`
+// (cost units), and at least two for the `tail` last sorted units that cost
+// at least `tail_min` (a cut adds a work item, whose K/V load and epilogue
+// cost about ten steps, so units small next to the per-SM share stay whole).
+__device__ __forceinline__ int unit_chunks(long long cost, long long target, int i, int n_units, int tail,
+                                           long long tail_min) {
+  long long c = (cost + target - 1) / target;
+  if (i >= n_units - tail && cost >= tail_min) c = c < 2 ? 2 : c;
+  return static_cast<int>(c > 1 ? c : 1);
+}
+
+__global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__ order, const int* __restrict__ ucost,
+                                                         const int* __restrict__ usteps, const int* __restrict__ key,
+                                                         int n_units, int expand,
+                                                         int num_sms, int max_slots, int* __restrict__ nchunk,
+                                                         int* __restrict__ item_start,
+                                                         int* __restrict__ split_start, int* __restrict__ n_work,
+                                                         int* __restrict__ run_first, int* __restrict__ run_of) {
   __shared__ long long red_ll[32];
   __shared__ int red[32];
   long long local = 0;
-  for (int u = threadIdx.x; u < n_units; u += blockDim.x) local += usteps[u];
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) local += ucost[u];
   const long long total = block_sum_ll(local, red_ll) * expand;
   long long target = total * 3 / (4LL * max(1, num_sms));
-  if (target < kMinChunkSteps) target = kMinChunkSteps;
-  for (int round = 0; round < 40; ++round) {  // grow chunks until the partial slots suffice
+  if (target < kMinChunkSteps * kCostDkv.full) target = kMinChunkSteps * kCostDkv.full;
+  int tail = (num_sms + expand - 1) / expand;  // units holding the last num_sms items
+  const long long share = total / max(1, num_sms);
+  const long long tail_min = max(static_cast<long long>(kMinChunkSteps) * kCostDkv.full, share / 4);
+  for (int round = 0; round < 80; ++round) {  // shrink the cuts until the partial slots suffice
     long long slots = 0;
-    for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
-      const long long c = (usteps[u] + target - 1) / target;
-      if (c > 1) slots += c * expand;
+    for (int i = threadIdx.x; i < n_units; i += blockDim.x) {
+      const int u = order[i];
+      const int c = unit_chunks(ucost[u], target, i, n_units, tail, tail_min);
+      if (c > 1) slots += static_cast<long long>(c) * expand;
     }
     if (block_sum_ll(slots, red_ll) <= max_slots) break;
-    target *= 2;
+    if (tail > 0) tail = tail / 2; else target *= 2;
   }
-  for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
-    const long long c = (usteps[u] + target - 1) / target;
-    nchunk[u] = static_cast<int>(c > 1 ? c : 1);
+  for (int i = threadIdx.x; i < n_units; i += blockDim.x) {
+    const int u = order[i];
+    nchunk[u] = unit_chunks(ucost[u], target, i, n_units, tail, tail_min);
   }
   __syncthreads();
-  int item_base = 0, slot_base = 0;
+  // runs: maximal stretches of sorted units with the same cost bucket and chunk count;
+  // run_of[i] = run of sorted unit i, run_first[r] = its first sorted unit
+  int run_base = 0;
   for (int i0 = 0; i0 < n_units; i0 += blockDim.x) {
     const int i = i0 + threadIdx.x;
-    int ni = 0, si = 0;
+    int head = 0;
     if (i < n_units) {
-      const int c = nchunk[order[i]];
-      ni = c * expand;
+      const int u = order[i];
+      head = (i == 0) || key[u] != key[order[i - 1]] || nchunk[u] != nchunk[order[i - 1]];
+    }
+    int tot;
+    const int pr = block_scan_excl(head, red, tot);
+    if (i < n_units) {
+      const int r = run_base + pr + head - 1;
+      run_of[i] = r;
+      if (head) run_first[r] = i;
+    }
+    run_base += tot;
+  }
+  const int n_runs = run_base;
+  __syncthreads();
+  int item_base = 0, slot_base = 0;
+  for (int r0 = 0; r0 < n_runs; r0 += blockDim.x) {
+    const int r = r0 + threadIdx.x;
+    int ni = 0, si = 0;
+    if (r < n_runs) {
+      const int first = run_first[r];
+      const int last = (r + 1 < n_runs) ? run_first[r + 1] : n_units;
+      const int c = nchunk[order[first]];
+      ni = c * expand * (last - first);
       si = (c > 1) ? ni : 0;
     }
     int tot_i, tot_s;
     const int pi = block_scan_excl(ni, red, tot_i);
     const int ps = block_scan_excl(si, red, tot_s);
-    if (i < n_units) {
-      item_start[i] = item_base + pi;
-      split_start[i] = slot_base + ps;
+    if (r < n_runs) {
+      item_start[r] = item_base + pi;
+      split_start[r] = slot_base + ps;
     }
     item_base += tot_i;
     slot_base += tot_s;
   }
   if (threadIdx.x == 0) {
-    item_start[n_units] = item_base;
-    *n_work = item_base;
+    item_start[n_runs] = item_base;
+    n_work[0] = item_base;
+    n_work[1] = n_runs;
   }
 }
 
 void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st) {
   note_launches(1);
-  split_dkv_kernel<<<1, 1024, 0, st>>>(wl.order, usteps, wl.n_sorted, wl.expand, num_sms, sp.max_slots, sp.nchunk,
-                                       sp.item_start, sp.split_start, sp.n_work);
+  split_dkv_kernel<<<1, 1024, 0, st>>>(wl.order, wl.cnt, usteps, wl.key, wl.n_sorted, wl.expand, num_sms,
+                                       sp.max_slots, sp.nchunk, sp.item_start, sp.split_start, sp.n_work,
+                                       sp.run_first, sp.run_of);
 }
 
 // ---------------------------------------------------------------- cost sort
 // Counting sort by descending cost in one block of 1024 threads.  Rows with
 // equal cost keep no particular order (the result does not depend on it).
-__global__ void __launch_bounds__(1024) sort_kernel(const int* __restrict__ cnt, int n, const uint32_t* __restrict__ hist,
+__global__ void __launch_bounds__(1024) sort_kernel(const int* __restrict__ key, int n, const uint32_t* __restrict__ hist,
                                                     int* __restrict__ order, int* __restrict__ counter) {
   __shared__ uint32_t start[kCostBuckets];
   __shared__ uint32_t warp_sums[32];
@@ -363,7 +461,7 @@ __global__ void __launch_bounds__(1024) sort_kernel(const int* __restrict__ cnt,
   }
   __syncthreads();
   for (int r = tid; r < n; r += blockDim.x) {
-    const int b = min(cnt[r], kCostBuckets - 1);
+    const int b = key[r];
     const uint32_t pos = atomicAdd(&start[b], 1u);
     order[pos] = r;
   }
@@ -372,7 +470,7 @@ __global__ void __launch_bounds__(1024) sort_kernel(const int* __restrict__ cnt,
 
 void launch_sort(const WorkList& wl, cudaStream_t st) {
   note_launches(1);
-  sort_kernel<<<1, 1024, 0, st>>>(wl.cnt, wl.n_sorted, wl.hist, wl.order, wl.counter);
+  sort_kernel<<<1, 1024, 0, st>>>(wl.key, wl.n_sorted, wl.hist, wl.order, wl.counter);
 }
 
 // ---------------------------------------------------------------- test hooks

@@ -97,7 +97,9 @@ def _split_cases():
     """Layouts where some dK/dV units are far longer than the per-SM share,
     so the planner cuts them into chunks whose partial sums are reduced:
     keys every query attends (global tokens), every unit long (FULL with all
-    query heads on one KV head), per-head block maps, one long document."""
+    query heads on one KV head), per-head block maps, one long document.  In
+    all of them the last units of the cost order are also cut in two (the
+    tail cut), so whole, long-unit and tail chunks meet in one launch."""
     from gen import MaskSpec, Problem, Segment
 
     out = [

@@ -12,9 +12,12 @@ PK = {"hbm_gbs": 6784.2, "bf16_tflops": 1937.2, "bf16_tflops_sustained": 1701.9}
 
 
 def test_peak_is_burst_only_when_the_clock_held_its_maximum():
-    held = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 3}
+    held = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 40, "reason_samples": {}}
     assert bench.tensor_peak(PK, "measured", held)[0] == PK["bf16_tflops"]
-    capped = dict(held, reasons=["sw_power_cap"])
+    # the power cap in a few samples: the clock still held; in a quarter or more: sustained
+    rare = dict(held, reasons=["sw_power_cap"], reason_samples={"sw_power_cap": 3})
+    assert bench.tensor_peak(PK, "measured", rare)[0] == PK["bf16_tflops"]
+    capped = dict(held, reasons=["sw_power_cap"], reason_samples={"sw_power_cap": 10})
     assert bench.tensor_peak(PK, "measured", capped)[0] == PK["bf16_tflops_sustained"]
     slow = dict(held, sm_mhz=1800.0)
     assert bench.tensor_peak(PK, "measured", slow)[0] == PK["bf16_tflops_sustained"]
@@ -52,3 +55,15 @@ def test_workload_lists():
     assert len(bench.workload_problems(workload="shards512k")) == 1
     assert [p.mask.kind for p in bench.workload_problems(only="CAUSAL,FULL")] == ["FULL", "CAUSAL"]
     assert set(bench.DROPOUT) <= set(bench.WORKLOADS)
+
+
+def test_clock_samples_parsed_with_reason_counts():
+    out = "\n".join([
+        "0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 2070, 2070, 1390.5, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 1395.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "garbage line",
+    ])
+    clk = bench.parse_clock_samples(out)
+    assert clk["samples"] == 3 and clk["sm_mhz"] == 2070.0 and clk["sm_max_mhz"] == 2070.0
+    assert clk["reasons"] == ["sw_power_cap"] and clk["reason_samples"] == {"sw_power_cap": 2}
