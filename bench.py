@@ -294,6 +294,33 @@ def parse_clock_samples(out: str):
             "reasons": sorted(counts), "samples": len(sm), "reason_samples": counts}
 
 
+# ------------------------------------------------------------------ host placement
+def gpu_local_cpus(dev_index: int):
+    """(CPUs local to the GPU, its NUMA node) from sysfs, or (None, None).
+    On a Grace host the pinned buffers of the end-to-end leg should live in
+    the memory of the CPU the GPU hangs off (NVLink-C2C), so the process is
+    bound to those CPUs before it allocates them (first touch places pages)."""
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader", "-i",
+                              str(dev_index)], capture_output=True, text=True, timeout=20).stdout.strip()
+        dom, rest = out.split(":", 1)
+        addr = f"{int(dom, 16):04x}:{rest.lower()}"
+        base = f"/sys/bus/pci/devices/{addr}"
+        cpus = set()
+        with open(f"{base}/local_cpulist") as f:
+            for part in f.read().strip().split(","):
+                if "-" in part:
+                    a, b = part.split("-")
+                    cpus.update(range(int(a), int(b) + 1))
+                elif part:
+                    cpus.add(int(part))
+        with open(f"{base}/numa_node") as f:
+            node = int(f.read().strip())
+        return (cpus or None), node
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None, None
+
+
 # ------------------------------------------------------------------ distributed helpers
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
@@ -508,6 +535,14 @@ def run_ours(args):
         # compute (several streams let several copy engines work at once).  One
         # timed region covers all steps, from the first input copy to the last
         # output byte.
+        local_cpus, numa_node = gpu_local_cpus(int(clocks.gpu))
+        bound, saved_cpus = False, os.sched_getaffinity(0)
+        if local_cpus:
+            try:
+                os.sched_setaffinity(0, local_cpus)
+                bound = True
+            except OSError:
+                pass
         copy = torch.cuda.Stream()  # host -> device inputs
         outq = [torch.cuda.Stream() for _ in range(4)]  # device -> host outputs, round robin over masks
         hosts_in = [t.cpu().pin_memory() for t in (q, k, v, do)]
@@ -562,10 +597,14 @@ def run_ours(args):
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
+        if bound:
+            os.sched_setaffinity(0, saved_cpus)  # the CPU baseline below uses every core again
         e_ms, e_flops = aggregate(t0.elapsed_time(t1), step_flops * args.steps, world, dev)
         e2e = {"value": e_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
                "outputs": args.e2e_outputs,
+               "host_binding": ({"cpus": len(local_cpus), "gpu_numa_node": numa_node} if bound else
+                                "not bound (GPU's local CPUs unknown)"),
                "copies": ("inputs on one copy stream, double-buffered across steps; dQ, dK, dV stored by the "
                           "kernels into mapped pinned host memory, " if mapped else
                           "inputs on one copy stream, double-buffered across steps; ") +

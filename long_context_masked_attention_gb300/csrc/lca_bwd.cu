@@ -62,8 +62,11 @@ __device__ __forceinline__ uint4 pack8(const float* v, float mul) {
 namespace dq {
 
 // Shared memory: Q and dO tiles of the item, a 3-slot K ring and a 2-slot V
-// ring.  TMEM: S [0,128), dP [128,256), dQ [256,384), and dS as bf16 in two
-// 64-column buffers [384,448), [448,512) that the dQ product reads directly.
+// ring.  TMEM: S [0,128), dP [128,256), dQ [256,384), dS as bf16 pairs in
+// [384,448), read by the dQ product directly, and the item's dO rows as bf16
+// pairs in [448,512): the compute warps copy them there from shared memory
+// at the start of each item, and dP = dO V^T takes its A operand from TMEM,
+// so each key tile's products read 32 KB less from shared memory.
 constexpr int kKRing = 3, kVRing = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kOffQ + kTile128;
@@ -75,7 +78,7 @@ constexpr int kSmemBytes = kOffCtl + 1024 + 1024;
 enum : int {
   B_QFULL = 0, B_QEMPTY,
   B_KFULL, B_KEMPTY = B_KFULL + kKRing, B_VFULL = B_KEMPTY + kKRing, B_VEMPTY = B_VFULL + kVRing,
-  B_SFULL = B_VEMPTY + kVRing, B_SEMPTY, B_DSFULL, B_DSEMPTY = B_DSFULL + 2, B_DQFULL = B_DSEMPTY + 2,
+  B_SFULL = B_VEMPTY + kVRing, B_SEMPTY, B_DSFULL, B_DSEMPTY, B_DQFULL, B_DOFULL,
   B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_DRAIN = B_ITEMPTY + 2, B_COUNT
 };
 
@@ -173,12 +176,12 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
   const uint32_t base = smem_u32(sm);
   // operand descriptors built once; every MMA below only adds a byte offset
   const uint64_t dQd = sdesc_sw128(base + kOffQ, 16, 1024);
-  const uint64_t dOd = sdesc_sw128(base + kOffDO, 16, 1024);
   const uint64_t dKk = sdesc_sw128(base + kOffK, 16, 1024);         // K ring, K-major
   const uint64_t dKn = sdesc_sw128(base + kOffK, kChunk128, 1024);  // K ring, N-major
   const uint64_t dVk = sdesc_sw128(base + kOffV, 16, 1024);
-  uint32_t tiles = 0;  // key tiles consumed (ring positions, dS buffers)
+  uint32_t tiles = 0;  // key tiles consumed (ring positions, dS phases)
   uint32_t sdp = 0;    // S/dP products issued (TMEM reuse count)
+  uint32_t do_items = 0;  // items whose dO rows were copied into TMEM
   for (int it = 0;; ++it) {
     const int slot = it & 1;
     if (!waitw(&bar[B_ITFULL + slot], (it >> 1) & 1, a, 120)) goto abort;
@@ -203,29 +206,30 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
             umma_ss(tbase + 0, desc_add(dQd, off), desc_add(dK, off), kIdesc128, ks > 0);
           }
           if (!waitw(&bar[B_VFULL + vr], (idx / kVRing) & 1, a, 124)) goto abort;
+          if (t == 0 && !waitw(&bar[B_DOFULL], do_items & 1, a, 126)) goto abort;  // dO rows in TMEM
           tc_fence_after();
           const uint64_t dV = desc_add(dVk, vr * kTile128);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (ks >> 2) * kChunk128 + (ks & 3) * 32;
-            umma_ss(tbase + 128, desc_add(dOd, off), desc_add(dV, off), kIdesc128, ks > 0);
+            umma_ts(tbase + 128, tbase + 448 + 8 * ks, desc_add(dV, off), kIdesc128, ks > 0);
           }
           umma_commit(&bar[B_SFULL]);
           ++sdp;
         }
         if (t >= 1) {  // dQ += dS K for key tile t-1, dS read from TMEM
           const uint32_t idx = tiles + t - 1;
-          const int db = idx & 1, kr = idx % kKRing;
-          if (!waitw(&bar[B_DSFULL + db], (idx >> 1) & 1, a, 125)) goto abort;
+          const int kr = idx % kKRing;
+          if (!waitw(&bar[B_DSFULL], idx & 1, a, 125)) goto abort;
           tc_fence_after();
           const uint64_t dK = desc_add(dKn, kr * kTile128);
-          const uint32_t tA = tbase + 384 + 64 * db;
+          const uint32_t tA = tbase + 384;
           const uint32_t acc0 = (t > 1) ? 1u : 0u;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             umma_ts(tbase + 256, tA + 8 * ks, desc_add(dK, ks * 2048), kIdescMN, ks > 0 ? 1u : acc0);
           }
-          umma_commit(&bar[B_DSEMPTY + db]);
+          umma_commit(&bar[B_DSEMPTY]);
           umma_commit(&bar[B_KEMPTY + kr]);
           if (t == n) umma_commit(&bar[B_DQFULL]);
         }
@@ -237,6 +241,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sm, uint6
       }
       if (n == 0) umma_commit(&bar[B_QEMPTY]);
       tiles += n;
+      do_items += (n > 0);
     }
   }
 abort:
@@ -265,6 +270,29 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
     if (!inf.valid) return;
+    if (inf.cnt > 0) {
+      // this item's dO rows into TMEM, the A operand of dP = dO V^T: thread
+      // (row, half) copies the row's 64 columns of its half from the
+      // 128-byte-swizzled tile (16-byte unit u of row r sits at u ^ (r % 8)).
+      // The previous item's last dP has completed: its S/dP commit was
+      // waited for before that item's last dS.
+      if (!waitw(&bar[B_QFULL], it & 1, a, 135)) return;
+      const uint8_t* src = sm + kOffDO + half * kChunk128 + row * 128;
+      uint32_t r[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 w = *reinterpret_cast<const uint4*>(src + ((u ^ (row & 7)) << 4));
+        r[4 * u] = w.x;
+        r[4 * u + 1] = w.y;
+        r[4 * u + 2] = w.z;
+        r[4 * u + 3] = w.w;
+      }
+      tmem_st32(tbase + tl + 448 + 32 * half, r);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[B_DOFULL]);
+    }
     const SegInfo sg = pv.segs[inf.seg];
     const int i = inf.qt * kTile + row;
     const bool valid = i < sg.q_len;
@@ -329,15 +357,15 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         const uint64_t ds = fmul2(pp, dd);
         pk[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
       }
-      // dS (bf16) into TMEM buffer db, this thread's 64 key columns = 32 packed columns
-      const int db = tiles & 1;
-      if (tiles >= 2 && !waitw(&bar[B_DSEMPTY + db], ((tiles >> 1) - 1) & 1, a, 132)) return;
+      // dS (bf16) into TMEM, this thread's 64 key columns = 32 packed columns,
+      // once the previous tile's dQ product has read the buffer
+      if (tiles >= 1 && !waitw(&bar[B_DSEMPTY], (tiles - 1) & 1, a, 132)) return;
       tc_fence_after();
-      tmem_st32(tbase + tl + 384 + 64 * db + 32 * half, pk);
+      tmem_st32(tbase + tl + 384 + 32 * half, pk);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[B_DSFULL + db]);
+      if (lane == 0) mbar_arrive(&bar[B_DSFULL]);
     }
     __nv_bfloat16* qrow = dQ + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + inf.head) * kHeadDim +
                           half * 64;
@@ -385,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < B_COUNT; ++b) mbar_init(&bar[b], 1);
     mbar_init(&bar[B_SEMPTY], 8);  // one arrival per compute warp
     mbar_init(&bar[B_DSFULL], 8);
-    mbar_init(&bar[B_DSFULL + 1], 8);
+    mbar_init(&bar[B_DOFULL], 8);
     mbar_init(&bar[B_ITEMPTY], 9);
     mbar_init(&bar[B_ITEMPTY + 1], 9);
     counts[0] = counts[1] = counts[2] = 0;

@@ -291,34 +291,55 @@ __device__ __forceinline__ uint32_t mask_bits_any(const MaskCtx& m, const SegInf
   return (m.kind == kFlashMask) ? mask_bits<true>(m, sg, hm, i, j0) : mask_bits<false>(m, sg, hm, i, j0);
 }
 
+// Class byte from the attended-cell facts of a tile (see classify_tile_warp).
+__device__ __forceinline__ uint32_t tile_class(bool any0, bool any1, bool all, bool inside) {
+  if (!any0 && !any1) return kTileEmpty;
+  if (all && inside) return kTileFull;
+  return kTilePartial | (any0 ? 0u : kHalf0Empty) | (any1 ? 0u : kHalf1Empty);
+}
+
+// Class of a 128x128 tile of a block-sparse map, computed by one thread: the
+// (query block, key block) pairs the tile overlaps are few (at most 5 x 5
+// for blocks of 32 or more keys and rows), so a thread reads their keep bits
+// itself and a warp classifies 32 tiles at once.
+__device__ __forceinline__ uint32_t classify_block_tile(const MaskCtx& m, const SegInfo& sg, int hm, int r0, int c0) {
+  const int r1 = min(r0 + kTile, sg.q_len), c1 = min(c0 + kTile, sg.k_len);
+  if (r1 <= r0 || c1 <= c0) return kTileEmpty;
+  const bool inside = (r0 + kTile <= sg.q_len) && (c0 + kTile <= sg.k_len);
+  const int rm = min(r0 + kTile / 2, r1);  // first row of the second half (r1 if it has none)
+  const int qbA = q_block_of(m, sg.q_off + r0), qbB = q_block_of(m, sg.q_off + r1 - 1);
+  const int kbA = k_block_of(m, sg.k_off + c0), kbB = k_block_of(m, sg.k_off + c1 - 1);
+  const int qbM0 = q_block_of(m, sg.q_off + rm - 1);                    // last block of half 0
+  const int qbM1 = (rm < r1) ? q_block_of(m, sg.q_off + rm) : qbB + 1;  // first block of half 1
+  bool any0 = false, any1 = false, all = true;
+  for (int qb = qbA; qb <= qbB; ++qb) {
+    for (int kb = kbA; kb <= kbB; ++kb) {
+      const bool kept = block_kept(m, hm, qb, kb);
+      any0 |= kept && qb <= qbM0;
+      any1 |= kept && qb >= qbM1;
+      all &= kept;
+    }
+  }
+  return tile_class(any0, any1, all, inside);
+}
+
 // Class of the 128x128 tile with rows [r0, r0+128) and keys [c0, c0+128) of
 // one segment: EMPTY if no valid cell is attended, FULL if the tile lies
 // inside the segment and every cell is attended, PARTIAL otherwise.  A
 // PARTIAL tile also carries kHalf0Empty / kHalf1Empty when no cell of its
 // rows [r0, r0+64) / [r0+64, r0+128) inside the segment is attended (the
 // dK/dV kernel skips such 64-row steps).  All 32 lanes of the warp must call
-// it; every lane gets the result.
+// it; every lane gets the result.  (Block-sparse maps: every lane evaluates
+// classify_block_tile, the per-thread form the planner uses.)
 __device__ __forceinline__ uint32_t classify_tile_warp(const MaskCtx& m, const SegInfo& sg, int hm, int r0, int c0) {
   const int lane = threadIdx.x & 31;
+  if (is_block_sparse(m.kind)) return classify_block_tile(m, sg, hm, r0, c0);
   const int r1 = min(r0 + kTile, sg.q_len), c1 = min(c0 + kTile, sg.k_len);
   if (r1 <= r0 || c1 <= c0) return kTileEmpty;
   const bool inside = (r0 + kTile <= sg.q_len) && (c0 + kTile <= sg.k_len);
   const int rm = min(r0 + kTile / 2, r1);  // first row of the second half (r1 if it has none)
   bool any0 = false, any1 = false, all = true;
-  if (is_block_sparse(m.kind)) {
-    const int qbA = q_block_of(m, sg.q_off + r0), qbB = q_block_of(m, sg.q_off + r1 - 1);
-    const int kbA = k_block_of(m, sg.k_off + c0), kbB = k_block_of(m, sg.k_off + c1 - 1);
-    const int qbM0 = q_block_of(m, sg.q_off + rm - 1);                    // last block of half 0
-    const int qbM1 = (rm < r1) ? q_block_of(m, sg.q_off + rm) : qbB + 1;  // first block of half 1
-    const int nq = qbB - qbA + 1, nk = kbB - kbA + 1;
-    for (int t = lane; t < nq * nk; t += 32) {
-      const int qb = qbA + t / nk;
-      const bool kept = block_kept(m, hm, qb, kbA + t % nk);
-      any0 |= kept && qb <= qbM0;
-      any1 |= kept && qb >= qbM1;
-      all &= kept;
-    }
-  } else if (m.kind == kFlashMask) {
+  if (m.kind == kFlashMask) {
     for (int c = c0 + lane; c < c1; c += 32) {
       const int4 b = __ldg(m.cols + sg.k_off + c);
       const int masked0 = col_masked_rows(b, r0, rm), masked1 = col_masked_rows(b, rm, r1);
@@ -337,9 +358,7 @@ __device__ __forceinline__ uint32_t classify_tile_warp(const MaskCtx& m, const S
   any0 = __any_sync(0xFFFFFFFFu, any0);
   any1 = __any_sync(0xFFFFFFFFu, any1);
   all = __all_sync(0xFFFFFFFFu, all);
-  if (!any0 && !any1) return kTileEmpty;
-  if (all && inside) return kTileFull;
-  return kTilePartial | (any0 ? 0u : kHalf0Empty) | (any1 ? 0u : kHalf1Empty);
+  return tile_class(any0, any1, all, inside);
 }
 
 }  // namespace lca

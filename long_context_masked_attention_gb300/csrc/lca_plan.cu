@@ -91,10 +91,33 @@ __global__ void classify_tiles_kernel(PlanView pv, uint8_t* __restrict__ tcls, l
   }
 }
 
+// Block-sparse maps: one thread per tile (classify_block_tile).
+__global__ void classify_block_tiles_kernel(PlanView pv, uint8_t* __restrict__ tcls, long long total) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < total; w += stride) {
+    const int hm = static_cast<int>(w / pv.dq_per_hm);
+    const long long t = w % pv.dq_per_hm;
+    int lo = 0, hi = pv.n_seg;  // last segment whose offset is <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pv.dq_off[mid] <= t) lo = mid; else hi = mid;
+    }
+    const SegInfo sg = pv.segs[lo];
+    const long long r = t - pv.dq_off[lo];
+    const int qt = static_cast<int>(r / sg.nk), kt = static_cast<int>(r % sg.nk);
+    tcls[w] = static_cast<uint8_t>(classify_block_tile(pv.mask, sg, hm, qt * kTile, kt * kTile));
+  }
+}
+
 void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st) {
   const long long total = static_cast<long long>(pv.hm_count) * pv.dq_per_hm;
   if (total == 0) return;
   note_launches(1);
+  if (is_block_sparse(pv.mask.kind)) {
+    const long long blocks = std::min<long long>((total + 255) / 256, 65536);
+    classify_block_tiles_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(pv, tcls, total);
+    return;
+  }
   const long long blocks = std::min<long long>((total + 7) / 8, 16384);
   classify_tiles_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(pv, tcls, total);
 }
