@@ -155,7 +155,12 @@ LCA_API lca_status lca_attn_fwd(const void* q, const void* k, const void* v, voi
 /* Backward (FlashAttention-2 核心优化, 反向传播: dK/dV per key tile, dQ in a
  * separate query-tile pass, D = rowsum(dO * O) prepass).  dout, q, k, v, o:
  * device bf16; lse: device float from lca_attn_fwd; dq, dk, dv: bf16 outputs
- * in device or mapped host memory (written, not accumulated). */
+ * in device or mapped host memory (written, not accumulated).
+ * The dK/dV pass runs on a stream the library owns (one per device, highest
+ * priority), forked from `stream` and joined back to it with events, so that
+ * the dQ pass runs beside it; all of the call's work still comes after the
+ * work queued on `stream` before the call and before the work queued after
+ * it. */
 LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);

@@ -487,6 +487,39 @@ int num_sms() {
   return n;
 }
 
+// The backward's dK/dV work runs on a library-owned stream of the highest
+// priority, forked from and joined back to the caller's stream by events, so
+// that the dQ pass (which does not read dK/dV) runs beside it: its lists are
+// built while dK/dV's are, and its persistent CTAs take the SMs that dK/dV
+// CTAs leave at the end of their work.  With dK/dV's stream at the higher
+// priority, dK/dV's CTAs are placed first when both kernels are ready, so the
+// shorter dQ pass fills the tail of the longer one.  One stream per device,
+// created on first use; calls that overlap on several caller streams share
+// it (their dK/dV parts run one after another).
+cudaStream_t side_stream(lca_status& err) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    err = LCA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev]) {
+    int lo = 0, hi = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&streams[dev], cudaStreamNonBlocking, hi);
+    if (e != cudaSuccess) {
+      err = cuda_fail("cudaStreamCreateWithPriority", e);
+      streams[dev] = nullptr;
+      return nullptr;
+    }
+  }
+  err = LCA_OK;
+  return streams[dev];
+}
+
 unsigned long long wait_limit_ns() {
   static unsigned long long v = 0;
   if (!v) {
@@ -872,6 +905,19 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
   ph = phase_begin(3, c.st);  // the tile classes serve both lists
   launch_classify(c.V, tcls, c.st);
   phase_end(ph, c.st);
+  // dK/dV on the side stream when both passes have work (see side_stream)
+  cudaStream_t sk = c.st;
+  cudaEvent_t ev_fork = nullptr, ev_planned = nullptr, ev_join = nullptr;
+  const bool fork = k_units > 0 && q_rows > 0;
+  if (fork) {
+    sk = side_stream(r);
+    if (r != LCA_OK) return r;
+    LCA_CUDA(cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming));
+    LCA_CUDA(cudaEventCreateWithFlags(&ev_planned, cudaEventDisableTiming));
+    LCA_CUDA(cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming));
+    LCA_CUDA(cudaEventRecord(ev_fork, c.st));
+    LCA_CUDA(cudaStreamWaitEvent(sk, ev_fork, 0));
+  }
   if (k_units > 0) {
     WorkList wl{};
     wl.cnt = reinterpret_cast<int*>(c.ws + c.L.k_ucost);
@@ -893,11 +939,12 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     sp.max_slots = c.L.k_max_slots;
     sp.run_first = reinterpret_cast<int*>(c.ws + c.L.k_runfirst);
     sp.run_of = reinterpret_cast<int*>(c.ws + c.L.k_runof);
-    ph = phase_begin(3, c.st);
-    launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, c.st);
-    launch_sort(wl, c.st);
-    launch_split_dkv(wl, usteps, sp, sms, c.st);
-    phase_end(ph, c.st);
+    ph = phase_begin(3, sk);
+    launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, sk);
+    launch_sort(wl, sk);
+    launch_split_dkv(wl, usteps, sp, sms, sk);
+    phase_end(ph, sk);
+    if (fork) LCA_CUDA(cudaEventRecord(ev_planned, sk));
     AttnArgs a = base_args(c, dr);
     a.cnt = wl.cnt;
     a.order = wl.order;
@@ -920,11 +967,12 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nlse2 = lse2;
     a.dk = dk;
     a.dv = dv;
-    a.prof = prof_slot(1, c.st);
-    ph = phase_begin(4, c.st);
-    launch_bwd_dkv(tq64, tk, tv, tdo64, a, sms, c.st);
-    launch_dkv_reduce(a, c.st);
-    phase_end(ph, c.st);
+    a.prof = prof_slot(1, sk);
+    ph = phase_begin(4, sk);
+    launch_bwd_dkv(tq64, tk, tv, tdo64, a, sms, sk);
+    launch_dkv_reduce(a, sk);
+    phase_end(ph, sk);
+    if (fork) LCA_CUDA(cudaEventRecord(ev_join, sk));
   }
   if (q_rows > 0) {
     WorkList wl{};
@@ -951,9 +999,19 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nlse2 = lse2;
     a.dq = dq;
     a.prof = prof_slot(2, c.st);
+    // the dQ kernel is queued once dK/dV's lists are built, so both kernels
+    // become ready together and the higher-priority dK/dV CTAs go first
+    if (fork) LCA_CUDA(cudaStreamWaitEvent(c.st, ev_planned, 0));
     ph = phase_begin(6, c.st);
     launch_bwd_dq(tq, tk, tv, tdo, a, sms, c.st);
     phase_end(ph, c.st);
+  }
+  if (fork) {
+    LCA_CUDA(cudaStreamWaitEvent(c.st, ev_join, 0));
+    // released by CUDA once recorded work completes
+    cudaEventDestroy(ev_fork);
+    cudaEventDestroy(ev_planned);
+    cudaEventDestroy(ev_join);
   }
   const size_t qrow = static_cast<size_t>(P.Hq) * kHeadDim * 2, krow = static_cast<size_t>(P.Hkv) * kHeadDim * 2;
   for (auto& gp : P.q_gaps) launch_zero16(static_cast<uint8_t*>(dq) + gp.first * qrow, gp.second * qrow, c.st);
