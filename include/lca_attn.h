@@ -160,7 +160,8 @@ LCA_API lca_status lca_attn_fwd(const void* q, const void* k, const void* v, voi
  * priority), forked from `stream` and joined back to it with events, so that
  * the dQ pass runs beside it; all of the call's work still comes after the
  * work queued on `stream` before the call and before the work queued after
- * it. */
+ * it.  While a profiling hook is on (lca_set_kernel_events or
+ * lca_set_cta_profile) the passes run one after another on `stream`. */
 LCA_API lca_status lca_attn_bwd(const void* dout, const void* q, const void* k, const void* v, const void* o,
                         const float* lse, void* dq, void* dk, void* dv, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);

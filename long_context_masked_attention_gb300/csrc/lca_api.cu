@@ -908,7 +908,11 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
   // dK/dV on the side stream when both passes have work (see side_stream)
   cudaStream_t sk = c.st;
   cudaEvent_t ev_fork = nullptr, ev_planned = nullptr, ev_join = nullptr;
-  const bool fork = k_units > 0 && q_rows > 0;
+  // with a profiling hook on (phase events or the CTA profile) the passes run
+  // one after another, so that each phase's events and each kernel's CTA
+  // records cover that kernel alone
+  const bool profiling = (g_ring.events != nullptr && g_ring.n_pairs > 0) || g_prof != nullptr;
+  const bool fork = k_units > 0 && q_rows > 0 && !profiling;
   if (fork) {
     sk = side_stream(r);
     if (r != LCA_OK) return r;
