@@ -279,6 +279,9 @@ lca_status validate(const lca_shape* sh, const lca_mask_desc* md, HostPlan& P) {
         m.kv_block = md->kv_block;
         m.n_qb = static_cast<int>(std::max<long long>(1, cdiv(P.Tq, md->q_block)));
         m.n_kb = static_cast<int>(std::max<long long>(1, cdiv(P.Tk, md->kv_block)));
+        m.aligned = (md->q_block % 32 == 0 && md->kv_block % 32 == 0) ? 1 : 0;
+        for (int s = 0; s < P.n_seg && m.aligned; ++s)
+          if (P.segs[s].q_off % 32 != 0 || P.segs[s].k_off % 32 != 0) m.aligned = 0;
       } else {
         if (!md->qb_bounds || !md->kb_bounds || md->n_qb < 1 || md->n_kb < 1) return LCA_ERR_INVALID_ARG;
         if (md->qb_bounds[0] != 0 || md->kb_bounds[0] != 0) return LCA_ERR_INVALID_ARG;

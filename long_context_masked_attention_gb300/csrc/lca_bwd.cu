@@ -249,8 +249,9 @@ abort:
   mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
 }
 
-template <bool kCols, bool kDrop>
+template <int kForm, bool kDrop>
 __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
+  constexpr bool kCols = kForm == kFormCols;
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
   const DropCtx dc = make_drop_ctx(a.drop_t);
@@ -331,10 +332,29 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_SEMPTY]);
       ++sdp;
+      // aligned block maps: one keep bit per 32-key chunk of the thread's
+      // half for the warp's 32 rows, when they and the tile's keys all lie
+      // inside the segment; a masked chunk's dS is written as zeros
+      bool blk = false;
+      uint32_t keep2 = 3u;
+      if constexpr (kForm == kFormBlocks) {
+        const int i0 = inf.qt * kTile + wq * 32;
+        blk = cls == kTilePartial && i0 + 32 <= sg.q_len && kt * kTile + kTile <= sg.k_len;
+        if (blk) {
+          const int qb = q_block_of(pv.mask, sg.q_off + i0);
+          keep2 = 0u;
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            keep2 |= block_kept(pv.mask, inf.hm, qb, k_block_of(pv.mask, sg.k_off + kt * kTile + half * 64 + 32 * c))
+                         ? 1u << c
+                         : 0u;
+        }
+      }
       if (cls == kTilePartial) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          const uint32_t bits = mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
+          const uint32_t bits = blk ? (((keep2 >> c) & 1u) ? ~0u : 0u)
+                                    : mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
           if (!__all_sync(0xFFFFFFFFu, bits == ~0u)) {  // the warp's 32 rows do not all keep the chunk
 #pragma unroll
             for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;
@@ -343,19 +363,22 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       }
       uint32_t pk[32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const uint64_t xx = ffma2(f2(s[2 * k], s[2 * k + 1]), sl2x2, nl2);
-        const uint64_t pp = f2(ex2_approx(f2lo(xx)), ex2_approx(f2hi(xx)));
-        uint64_t dd;
-        if (kDrop) {  // dS' = P (Z dP~ - kp D)
-          const float z0 = ((kb[k >> 4] >> ((2 * k) & 31)) & 1u) ? dp[2 * k] : 0.f;
-          const float z1 = ((kb[k >> 4] >> ((2 * k + 1) & 31)) & 1u) ? dp[2 * k + 1] : 0.f;
-          dd = fadd2(f2(z0, z1), nD2);
-        } else {
-          dd = fadd2(f2(dp[2 * k], dp[2 * k + 1]), nD2);
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int k = 16 * c; k < 16 * c + 16; ++k) {
+          const uint64_t xx = ffma2(f2(s[2 * k], s[2 * k + 1]), sl2x2, nl2);
+          const uint64_t pp = f2(ex2_approx(f2lo(xx)), ex2_approx(f2hi(xx)));
+          uint64_t dd;
+          if (kDrop) {  // dS' = P (Z dP~ - kp D)
+            const float z0 = ((kb[k >> 4] >> ((2 * k) & 31)) & 1u) ? dp[2 * k] : 0.f;
+            const float z1 = ((kb[k >> 4] >> ((2 * k + 1) & 31)) & 1u) ? dp[2 * k + 1] : 0.f;
+            dd = fadd2(f2(z0, z1), nD2);
+          } else {
+            dd = fadd2(f2(dp[2 * k], dp[2 * k + 1]), nD2);
+          }
+          const uint64_t ds = fmul2(pp, dd);
+          pk[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
         }
-        const uint64_t ds = fmul2(pp, dd);
-        pk[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
       }
       // dS (bf16) into TMEM, this thread's 64 key columns = 32 packed columns,
       // once the previous tile's dQ product has read the buffer
@@ -394,7 +417,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   }
 }
 
-template <bool kCols, bool kDrop>
+template <int kForm, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
@@ -429,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
-    compute<kCols, kDrop>(a, sm, bar, items, tbase);
+    compute<kForm, kDrop>(a, sm, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -768,8 +791,9 @@ abort:
   mbar_wait(&bar[B_DRAIN], 0, nullptr, 100000000ull, 0, 0);
 }
 
-template <bool kCols, bool kDrop>
+template <int kForm, bool kDrop>
 __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t* bar, Item* items, uint32_t tbase) {
+  constexpr bool kCols = kForm == kFormCols;
   const PlanView& pv = a.pv;
   const DropCtx dc = make_drop_ctx(a.drop_t);
   const float dv_scale = kDrop ? a.drop_inv : 1.f, dk_scale = kDrop ? a.scale * a.drop_inv : a.scale;
@@ -802,15 +826,21 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       // thread's key: FlashMask reads them off the key's column bounds; the
       // other families evaluate one query row per lane over the warp's 32
       // keys and transpose the 32 x 32 bits across the warp
+      // (aligned block maps: the warp's 32 keys and 32 queries lie in one
+      // block pair when both are inside the segment; a masked pair writes
+      // zero P^T and dS^T without reading S^T, dP^T)
       uint32_t mb = ~0u;
+      bool skip = false;
       if (cls == kTilePartial) {
         const SegInfo sg = meta_s->sg;
         const int i0 = meta_s->r0 + 32 * half;
+        const int j0 = inf.kt * kTile + wq * 32;
         if constexpr (kCols) {
           mb = flashmask_key_bits(pv.mask, sg, inf.kt * kTile + j, i0);
+        } else if (kForm == kFormBlocks && i0 + 32 <= sg.q_len && j0 + 32 <= sg.k_len) {
+          skip = !block_kept(pv.mask, meta_s->hm, q_block_of(pv.mask, sg.q_off + i0), k_block_of(pv.mask, sg.k_off + j0));
         } else {
-          mb = warp_transpose_bits(mask_bits<false>(pv.mask, sg, meta_s->hm, i0 + lane, inf.kt * kTile + wq * 32),
-                                   lane);
+          mb = warp_transpose_bits(mask_bits<false>(pv.mask, sg, meta_s->hm, i0 + lane, j0), lane);
         }
       }
       uint32_t kb = ~0u;  // dropout keep bits: bit k = query 32*half + k for this thread's key
@@ -823,38 +853,43 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       }
       if (!waitw(&bar[B_SFULL + b], (steps >> 1) & 1, a, 231)) return;
       tc_fence_after();
-      float sv[32], dp[32];
-      {
-        uint32_t r[32];
-        tmem_ld32(tbase + tl + 64 * b + 32 * half, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) sv[k] = __uint_as_float(r[k]);
-        tmem_ld32(tbase + tl + 128 + 64 * b + 32 * half, r);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
-      }
-      tmem_ld_wait();
-      if (cls == kTilePartial && !__all_sync(0xFFFFFFFFu, mb == ~0u)) {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) sv[k] = ((mb >> k) & 1u) ? sv[k] : -INFINITY;
-      }
       uint32_t pp[16], pd[16];
-      // the staged statistics of this thread's 32 queries as packed pairs
-      const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s_nlse2 + 32 * half);
-      const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s_nD + 32 * half);
+      if (kForm == kFormBlocks && skip) {  // warp-uniform
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint64_t xx = ffma2(f2(sv[2 * k], sv[2 * k + 1]), sl2x2, nl2[k]);
-        const float p0 = ex2_approx(f2lo(xx)), p1 = ex2_approx(f2hi(xx));
-        if (kDrop) {  // P~ = P Z for dV; dS' = P Z dP~ - P kp D for dK
-          const float pz0 = ((kb >> (2 * k)) & 1u) ? p0 : 0.f, pz1 = ((kb >> (2 * k + 1)) & 1u) ? p1 : 0.f;
-          pp[k] = pack_bf16x2(pz0, pz1);
-          const uint64_t pnd = fmul2(f2(p0, p1), nd2[k]);
-          pd[k] = pack_bf16x2(fmaf(pz0, dp[2 * k], f2lo(pnd)), fmaf(pz1, dp[2 * k + 1], f2hi(pnd)));
-        } else {
-          pp[k] = pack_bf16x2(p0, p1);
-          const uint64_t ds = fmul2(f2(p0, p1), fadd2(f2(dp[2 * k], dp[2 * k + 1]), nd2[k]));
-          pd[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
+        for (int k = 0; k < 16; ++k) pp[k] = pd[k] = 0u;
+      } else {
+        float sv[32], dp[32];
+        {
+          uint32_t r[32];
+          tmem_ld32(tbase + tl + 64 * b + 32 * half, r);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) sv[k] = __uint_as_float(r[k]);
+          tmem_ld32(tbase + tl + 128 + 64 * b + 32 * half, r);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) dp[k] = __uint_as_float(r[k]);
+        }
+        tmem_ld_wait();
+        if (cls == kTilePartial && !__all_sync(0xFFFFFFFFu, mb == ~0u)) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) sv[k] = ((mb >> k) & 1u) ? sv[k] : -INFINITY;
+        }
+        // the staged statistics of this thread's 32 queries as packed pairs
+        const uint64_t* nl2 = reinterpret_cast<const uint64_t*>(s_nlse2 + 32 * half);
+        const uint64_t* nd2 = reinterpret_cast<const uint64_t*>(s_nD + 32 * half);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint64_t xx = ffma2(f2(sv[2 * k], sv[2 * k + 1]), sl2x2, nl2[k]);
+          const float p0 = ex2_approx(f2lo(xx)), p1 = ex2_approx(f2hi(xx));
+          if (kDrop) {  // P~ = P Z for dV; dS' = P Z dP~ - P kp D for dK
+            const float pz0 = ((kb >> (2 * k)) & 1u) ? p0 : 0.f, pz1 = ((kb >> (2 * k + 1)) & 1u) ? p1 : 0.f;
+            pp[k] = pack_bf16x2(pz0, pz1);
+            const uint64_t pnd = fmul2(f2(p0, p1), nd2[k]);
+            pd[k] = pack_bf16x2(fmaf(pz0, dp[2 * k], f2lo(pnd)), fmaf(pz1, dp[2 * k + 1], f2hi(pnd)));
+          } else {
+            pp[k] = pack_bf16x2(p0, p1);
+            const uint64_t ds = fmul2(f2(p0, p1), fadd2(f2(dp[2 * k], dp[2 * k + 1]), nd2[k]));
+            pd[k] = pack_bf16x2(f2lo(ds), f2hi(ds));
+          }
         }
       }
       __syncwarp();
@@ -929,7 +964,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
   }
 }
 
-template <bool kCols, bool kDrop>
+template <int kForm, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const AttnArgs a) {
@@ -962,11 +997,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   if (warp == 9) {
-    producer<kCols>(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items, counts);
+    producer<kForm == kFormCols>(a, &tmQ, &tmK, &tmV, &tmDO, sm, bar, items, counts);
   } else if (warp == 8) {
     mma_issuer(a, sm, bar, items, tbase);
   } else {
-    compute<kCols, kDrop>(a, sm, bar, items, tbase);
+    compute<kForm, kDrop>(a, sm, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -1025,47 +1060,55 @@ void launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const AttnArgs& a, int num_sms, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(dq::dq_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
-    cudaFuncSetAttribute(dq::dq_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
-    cudaFuncSetAttribute(dq::dq_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
-    cudaFuncSetAttribute(dq::dq_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<kFormSpans, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<kFormCols, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<kFormBlocks, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<kFormSpans, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
+    cudaFuncSetAttribute(dq::dq_kernel<kFormCols, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dq::kSmemBytes);
     configured = true;
   }
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
   const bool cols = a.pv.mask.kind == kFlashMask, drop = a.drop_t > 0;
+  const bool blocks = a.pv.mask.kind == kBlockSparseUniform && a.pv.mask.aligned;
   if (cols && drop)
-    dq::dq_kernel<true, true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dq::dq_kernel<kFormCols, true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
   else if (cols)
-    dq::dq_kernel<true, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
-  else if (drop)
-    dq::dq_kernel<false, true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dq::dq_kernel<kFormCols, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (drop)  // dropout on a block map takes the per-row mask words
+    dq::dq_kernel<kFormSpans, true><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (blocks)
+    dq::dq_kernel<kFormBlocks, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
   else
-    dq::dq_kernel<false, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dq::dq_kernel<kFormSpans, false><<<grid, kThreads, dq::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
 }
 
 void launch_bwd_dkv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
                     const AttnArgs& a, int num_sms, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(dkv::dkv_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
-    cudaFuncSetAttribute(dkv::dkv_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
-    cudaFuncSetAttribute(dkv::dkv_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
-    cudaFuncSetAttribute(dkv::dkv_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<kFormSpans, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<kFormCols, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<kFormBlocks, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<kFormSpans, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
+    cudaFuncSetAttribute(dkv::dkv_kernel<kFormCols, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv::kSmemBytes);
     configured = true;
   }
   // the item count is known on the device only (split pass); surplus CTAs find no work and exit
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
   const bool cols = a.pv.mask.kind == kFlashMask, drop = a.drop_t > 0;
+  const bool blocks = a.pv.mask.kind == kBlockSparseUniform && a.pv.mask.aligned;
   if (cols && drop)
-    dkv::dkv_kernel<true, true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dkv::dkv_kernel<kFormCols, true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
   else if (cols)
-    dkv::dkv_kernel<true, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
-  else if (drop)
-    dkv::dkv_kernel<false, true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dkv::dkv_kernel<kFormCols, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (drop)  // dropout on a block map takes the per-row mask words
+    dkv::dkv_kernel<kFormSpans, true><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+  else if (blocks)
+    dkv::dkv_kernel<kFormBlocks, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
   else
-    dkv::dkv_kernel<false, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
+    dkv::dkv_kernel<kFormSpans, false><<<grid, kThreads, dkv::kSmemBytes, st>>>(tq, tk, tv, tdo, a);
 }
 
 void launch_dkv_reduce(const AttnArgs& a, cudaStream_t st) {

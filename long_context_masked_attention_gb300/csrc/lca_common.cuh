@@ -75,7 +75,16 @@ struct MaskCtx {
   const int* kb_start;    // variable: key block bounds [n_kb + 1]
   const int* qb_start;    // variable: query block bounds [n_qb + 1]
   const int4* cols;       // FlashMask: {lts, lte, uts, ute} per global key [Tk]
+  // uniform block map whose blocks and segment starts are multiples of 32:
+  // every 32 rows x 32 keys of a tile (a warp's rows, a 32-column chunk)
+  // then lie in one (query block, key block) pair
+  int aligned;
 };
+
+// Mask forms the attention kernels are compiled for: the interval families
+// and generic block maps (mask words per row), FlashMask's column bounds,
+// and aligned uniform block maps (one keep bit per warp and 32-key chunk).
+enum MaskForm : int { kFormSpans = 0, kFormCols = 1, kFormBlocks = 2 };
 
 __host__ __device__ __forceinline__ bool is_block_sparse(int kind) {
   return kind == kBlockSparseUniform || kind == kBlockSparseVariable;

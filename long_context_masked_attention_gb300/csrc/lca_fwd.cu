@@ -377,8 +377,60 @@ __device__ __forceinline__ float tile_exp(uint32_t tS, const uint32_t (&mb)[4], 
   return f2lo(t) + f2hi(t);
 }
 
-template <bool kCols, bool kDrop>
+// Aligned uniform block maps: a warp's 32 rows and a 32-column chunk lie in
+// one (query block, key block) pair, so the chunk is kept or masked for the
+// whole warp (bit c of keep4).  Masked chunks are neither loaded nor
+// exponentiated (their P is written as 0); kept ones need no selects.
+__device__ __forceinline__ float tile_row_max_blk(uint32_t tS, uint32_t keep4) {
+  float mp[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mp[j] = -INFINITY;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    if (!((keep4 >> c) & 1u)) continue;  // warp-uniform
+    uint32_t r[32];
+    tmem_ld32(tS + 32 * c, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      mp[j] = fmax3(mp[j], fmax3(__uint_as_float(r[j]), __uint_as_float(r[8 + j]), __uint_as_float(r[16 + j])),
+                    __uint_as_float(r[24 + j]));
+  }
+  return fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+}
+
+__device__ __forceinline__ float tile_exp_blk(uint32_t tS, uint32_t keep4, float sl2, float base) {
+  const uint64_t sl2x2 = f2(sl2, sl2), nb2 = f2(-base, -base);
+  uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t pk[16];
+    if ((keep4 >> c) & 1u) {  // warp-uniform
+      uint32_t r[32];
+      tmem_ld32(tS + 32 * c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint64_t xx = ffma2(f2(__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])), sl2x2, nb2);
+        const uint64_t pp = f2(ex2_approx(f2lo(xx)), ex2_approx(f2hi(xx)));
+        acc[k & 3] = fadd2(acc[k & 3], pp);
+        pk[k] = pack_bf16x2(f2lo(pp), f2hi(pp));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) pk[k] = 0u;
+    }
+    // P of chunk c goes over columns 16c..16c+15, which belong to chunks
+    // already read or not needed
+    tmem_st16(tS + 16 * c, pk);
+  }
+  const uint64_t t = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+  return f2lo(t) + f2hi(t);
+}
+
+template <int kForm, bool kDrop>
 __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* bar, Item* items, uint32_t tbase) {
+  constexpr bool kCols = kForm == kFormCols;
   const PlanView& pv = a.pv;
   const uint32_t* entries = static_cast<const uint32_t*>(a.entries);
   const int wq = (threadIdx.x >> 5) & 3;
@@ -412,14 +464,29 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       const int kt = static_cast<int>(e & 0xFFFFFFu);
       // mask words of a partial tile, computed while S is still being produced
       uint32_t mb[4] = {~0u, ~0u, ~0u, ~0u};
-      if (cls == kTilePartial) {
+      // aligned block maps: one keep bit per 32-key chunk for the warp's rows,
+      // when the warp's rows and the tile's keys all lie inside the segment
+      bool blk = false;
+      uint32_t keep4 = 0;
+      if constexpr (kForm == kFormBlocks) {
+        const int i0 = i - lane;  // the warp's first row
+        blk = cls == kTilePartial && i0 + 32 <= sg.q_len && kt * kTile + kTile <= sg.k_len;
+        if (blk) {
+          const int qb = q_block_of(pv.mask, sg.q_off + i0);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            keep4 |= block_kept(pv.mask, inf.hm, qb, k_block_of(pv.mask, sg.k_off + kt * kTile + 32 * c)) ? 1u << c : 0u;
+        }
+      }
+      if (cls == kTilePartial && !blk) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) mb[c] = mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
       }
       if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
       ++s_cons;
       tc_fence_after();
-      const float mx = (cls == kTilePartial) ? tile_row_max<true>(tS, mb) : tile_row_max<false>(tS, mb);
+      const float mx = blk ? tile_row_max_blk(tS, keep4)
+                           : ((cls == kTilePartial) ? tile_row_max<true>(tS, mb) : tile_row_max<false>(tS, mb));
       const float m_new = fmaxf(m_use, mx * sl2);
       float factor = 1.f;
       bool need = false;
@@ -434,9 +501,12 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       // columns of S_x in TMEM (the A operand of O_x += P_x V)
       const float base = (m_use == -INFINITY) ? 0.f : m_use;
       const uint32_t grow = static_cast<uint32_t>(sg.q_off + i), g0 = static_cast<uint32_t>(kt * 8);
-      const float sum = (cls == kTilePartial)
-                            ? tile_exp<true, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0)
-                            : tile_exp<false, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0);
+      float sum;
+      if (blk)
+        sum = tile_exp_blk(tS, keep4, sl2, base);
+      else
+        sum = (cls == kTilePartial) ? tile_exp<true, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0)
+                                    : tile_exp<false, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0);
       l = l * factor + sum;
       if (__any_sync(0xFFFFFFFFu, need)) {
         // the previous O_x += P_x V must have finished before O_x is rescaled
@@ -495,7 +565,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
   }
 }
 
-template <bool kCols, bool kDrop>
+template <int kForm, bool kDrop>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const AttnArgs a) {
@@ -539,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 8) {
     mma_issuer(a, sQ, sKV, bar, items, tbase);
   } else {
-    softmax_wg<kCols, kDrop>(a, warp >> 2, bar, items, tbase);
+    softmax_wg<kForm, kDrop>(a, warp >> 2, bar, items, tbase);
   }
   tc_fence_before();
   __syncthreads();
@@ -556,23 +626,27 @@ void launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap&
                 cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    cudaFuncSetAttribute(fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    cudaFuncSetAttribute(fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    cudaFuncSetAttribute(fwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<kFormSpans, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<kFormCols, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<kFormBlocks, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<kFormSpans, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(fwd_kernel<kFormCols, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     configured = true;
   }
   const int grid = max(1, min(num_sms, a.n_work));
   note_launches(1);
   const bool cols = a.pv.mask.kind == kFlashMask, drop = a.drop_t > 0;
+  const bool blocks = a.pv.mask.kind == kBlockSparseUniform && a.pv.mask.aligned;
   if (cols && drop)
-    fwd_kernel<true, true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+    fwd_kernel<kFormCols, true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
   else if (cols)
-    fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
-  else if (drop)
-    fwd_kernel<false, true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+    fwd_kernel<kFormCols, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  else if (drop)  // dropout on a block map takes the per-row mask words
+    fwd_kernel<kFormSpans, true><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+  else if (blocks)
+    fwd_kernel<kFormBlocks, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
   else
-    fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
+    fwd_kernel<kFormSpans, false><<<grid, kThreads, kSmemBytes, st>>>(tq, tk, tv, a);
 }
 
 }  // namespace lca

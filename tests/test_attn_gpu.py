@@ -254,3 +254,59 @@ def test_backward_on_a_side_stream_is_ordered(lca):
     torch.cuda.synchronize()
     for c, ref in zip(copies, (dq0, dk0, dv0)):
         assert torch.equal(c, ref)
+
+
+def _aligned_block_cases():
+    """Uniform block maps whose blocks and segment starts are multiples of 32
+    (the forward's per-warp keep-bit form), with ragged tails and several
+    segments, and the same map with a segment start off the 32 grid (the
+    per-row mask-word form)."""
+    from gen import MaskSpec, Problem, Segment, uniform_block_map
+
+    r = np.random.Generator(np.random.PCG64(71))
+    out = []
+    for b, T, segs, name in [
+        (32, 1000, [(0, 1000, 0, 1000)], "b32_one"),
+        (96, 960, [(0, 480, 0, 480), (512, 448, 512, 448)], "b96_two_aligned"),
+        (96, 960, [(0, 470, 0, 470), (490, 470, 490, 470)], "b96_two_unaligned"),
+        (64, 1100, [(64, 700, 0, 1100)], "b64_offset_q"),
+    ]:
+        n = -(-T // b)
+        rp, ci = uniform_block_map(n, n, 4, r)
+        spec = MaskSpec("BLOCK_SPARSE_UNIFORM", q_block=b, kv_block=b, heads_in_map=4, blk_row_ptr=rp, blk_col_idx=ci)
+        out.append(Problem("aligned_" + name, T, T, 4, 2, 128, [Segment(*s) for s in segs], spec, 72))
+    return out
+
+
+ALIGNED = _aligned_block_cases()
+
+
+@pytest.mark.parametrize("prob", ALIGNED, ids=[p.name for p in ALIGNED])
+def test_aligned_block_map_parity(lca, prob):
+    _parity(lca, prob)
+
+
+def test_aligned_block_map_matches_variable_form(lca):
+    """The keep-bit form gives the same forward and backward, bit for bit, as
+    the same map stated as variable blocks (which always takes per-row mask
+    words): the masked 32-key chunks it skips contribute exact zeros there."""
+    import copy
+
+    from gen import MaskSpec
+
+    for prob in ALIGNED[:2]:
+        m = prob.mask
+        n = (len(m.blk_row_ptr) - 1) // 4  # block rows per map head (4 heads in the map)
+        bounds = (np.arange(n + 1) * m.q_block).astype(np.int32)
+        var = copy.copy(prob)
+        var.mask = MaskSpec("BLOCK_SPARSE_VARIABLE", qb_bounds=bounds, kb_bounds=bounds, heads_in_map=4,
+                            blk_row_ptr=m.blk_row_ptr, blk_col_idx=m.blk_col_idx)
+        q, k, v, do = make_tensors(prob)
+        o1, l1 = run_fwd(lca, prob, q, k, v)
+        o2, l2 = run_fwd(lca, var, q, k, v)
+        assert np.array_equal(to_np(o1), to_np(o2)), prob.name
+        assert np.array_equal(to_np(l1), to_np(l2)), prob.name
+        g1 = run_bwd(lca, prob, q, k, v, do, o1, l1)
+        g2 = run_bwd(lca, var, q, k, v, do, o1, l1)
+        for name, x, y in zip(("dq", "dk", "dv"), g1, g2):
+            assert np.array_equal(to_np(x), to_np(y)), (prob.name, name)
