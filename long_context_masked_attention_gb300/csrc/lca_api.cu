@@ -899,18 +899,17 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
   if (r != LCA_OK) return r;
   float* D = reinterpret_cast<float*>(c.ws + c.L.D);
   float* lse2 = reinterpret_cast<float*>(c.ws + c.L.lse2);
-  int ph = phase_begin(2, c.st);
-  launch_d_prepass(o, dout, lse, D, lse2, P.Tq, P.Hq, dr.keep, c.st);
-  phase_end(ph, c.st);
   uint32_t* hist = reinterpret_cast<uint32_t*>(c.ws + c.L.hist);
   int* counters = reinterpret_cast<int*>(c.ws + c.L.counters);
   uint8_t* tcls = c.ws + c.L.tcls;
-  ph = phase_begin(3, c.st);  // the tile classes serve both lists
+  int ph = phase_begin(3, c.st);  // the tile classes serve both lists
   launch_classify(c.V, tcls, c.st);
   phase_end(ph, c.st);
-  // dK/dV on the side stream when both passes have work (see side_stream)
+  // dK/dV on the side stream when both passes have work (see side_stream):
+  // its lists are built while the D prepass streams O and dO on the caller's
+  // stream, and its kernel starts once both are done
   cudaStream_t sk = c.st;
-  cudaEvent_t ev_fork = nullptr, ev_planned = nullptr, ev_join = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_pre = nullptr, ev_planned = nullptr, ev_join = nullptr;
   // with a profiling hook on (phase events or the CTA profile) the passes run
   // one after another, so that each phase's events and each kernel's CTA
   // records cover that kernel alone
@@ -920,11 +919,16 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     sk = side_stream(r);
     if (r != LCA_OK) return r;
     LCA_CUDA(cudaEventCreateWithFlags(&ev_fork, cudaEventDisableTiming));
+    LCA_CUDA(cudaEventCreateWithFlags(&ev_pre, cudaEventDisableTiming));
     LCA_CUDA(cudaEventCreateWithFlags(&ev_planned, cudaEventDisableTiming));
     LCA_CUDA(cudaEventCreateWithFlags(&ev_join, cudaEventDisableTiming));
     LCA_CUDA(cudaEventRecord(ev_fork, c.st));
     LCA_CUDA(cudaStreamWaitEvent(sk, ev_fork, 0));
   }
+  ph = phase_begin(2, c.st);
+  launch_d_prepass(o, dout, lse, D, lse2, P.Tq, P.Hq, dr.keep, c.st);
+  phase_end(ph, c.st);
+  if (fork) LCA_CUDA(cudaEventRecord(ev_pre, c.st));
   if (k_units > 0) {
     WorkList wl{};
     wl.cnt = reinterpret_cast<int*>(c.ws + c.L.k_ucost);
@@ -975,6 +979,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.dk = dk;
     a.dv = dv;
     a.prof = prof_slot(1, sk);
+    if (fork) LCA_CUDA(cudaStreamWaitEvent(sk, ev_pre, 0));  // -D and -LSE*log2(e)
     ph = phase_begin(4, sk);
     launch_bwd_dkv(tq64, tk, tv, tdo64, a, sms, sk);
     launch_dkv_reduce(a, sk);
@@ -1017,6 +1022,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     LCA_CUDA(cudaStreamWaitEvent(c.st, ev_join, 0));
     // released by CUDA once recorded work completes
     cudaEventDestroy(ev_fork);
+    cudaEventDestroy(ev_pre);
     cudaEventDestroy(ev_planned);
     cudaEventDestroy(ev_join);
   }
