@@ -655,6 +655,7 @@ AttnArgs base_args(const Call& c, const Drop& dr) {
   a.drop_t = dr.t;
   a.drop_inv = dr.inv;
   a.drop_keys = philox_round_keys(dr.seed);
+  a.row_group = 1;
   return a;
 }
 
@@ -1007,6 +1008,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(q_rows * wl.expand);
+    a.row_group = (P.Hq == P.Hkv && wl.expand > 1) ? kMhaRowGroup : 1;
     a.nD = D;
     a.nlse2 = lse2;
     a.dq = dq;

@@ -107,14 +107,16 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       Item inf;
       inf.valid = 0;
       if (w < a.n_work) {
-        const int row = a.order[w / a.expand];
+        int sorted_row, head;
+        item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
+        const int row = a.order[sorted_row];
         const int hm = row / pv.R128, rr = row % pv.R128;
         const int s = find_bucket(pv.q128_start, pv.n_seg, rr);
         inf.valid = 1;
         inf.seg = s;
         inf.qt = rr - pv.q128_start[s];
         inf.hm = hm;
-        inf.head = (pv.hm_count == 1) ? (w % a.expand) : hm;
+        inf.head = (pv.hm_count == 1) ? head : hm;
         inf.cnt = a.cnt[row];
         inf.ebase = hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(inf.qt) * pv.segs[s].nk;
       }

@@ -213,6 +213,20 @@ __device__ __forceinline__ int span_count(const Span& s) {
   return n0 + n1 - both;
 }
 
+// Work item w of a query-major list: `rows` cost-sorted rows, each run for
+// `expand` heads.  Rows are taken in groups of `group`, and a group's rows
+// run head by head, so that the items in flight at once cover a few heads
+// (K/V tiles shared in L2 when every head has its own K/V) while the order
+// stays longest first up to the cost spread inside a group.  group = 1 is
+// the plain order: row by row, all heads of a row together.
+__device__ __forceinline__ void item_of(int w, int rows, int expand, int group, int& row, int& head) {
+  const int base = (w / (group * expand)) * group;
+  const int n = min(group, rows - base);
+  const int local = w - base * expand;
+  head = local / n;
+  row = base + local % n;
+}
+
 // ---------------------------------------------------------------- block-sparse
 __device__ __forceinline__ int q_block_of(const MaskCtx& m, int gq) {
   return (m.kind == kBlockSparseUniform) ? gq / m.q_block : m.qb_of[gq];

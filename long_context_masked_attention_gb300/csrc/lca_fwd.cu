@@ -111,14 +111,16 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       Item inf;
       inf.valid = 0;
       if (w < a.n_work) {
-        const int row = a.order[w / a.expand];
+        int sorted_row, head;
+        item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
+        const int row = a.order[sorted_row];
         const int hm = row / pv.R256, rr = row % pv.R256;
         const int s = find_bucket(pv.q256_start, pv.n_seg, rr);
         inf.valid = 1;
         inf.seg = s;
         inf.qb = rr - pv.q256_start[s];
         inf.hm = hm;
-        inf.head = (pv.hm_count == 1) ? (w % a.expand) : hm;
+        inf.head = (pv.hm_count == 1) ? head : hm;
         inf.cnt = a.cnt[row];
         inf.ebase = hm * pv.fwd_per_hm + pv.fwd_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk;
       }
