@@ -299,6 +299,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     const SegInfo sg = pv.segs[inf.seg];
     const int i = inf.qt * kTile + row;
     const bool valid = i < sg.q_len;
+    const Span row_sp = row_span(pv.mask, sg, i);  // interval families: the row's keys, for every tile
     const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
     const uint64_t nl2 = f2(valid ? a.nlse2[stat] : -INFINITY, valid ? a.nlse2[stat] : -INFINITY);  // -LSE2, twice
     const float nDv = valid ? a.nD[stat] : 0.f;
@@ -356,7 +357,8 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const uint32_t bits = blk ? (((keep2 >> c) & 1u) ? ~0u : 0u)
-                                    : mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c);
+                                    : mask_bits_row<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c,
+                                                           row_sp);
           if (!__all_sync(0xFFFFFFFFu, bits == ~0u)) {  // the warp's 32 rows do not all keep the chunk
 #pragma unroll
             for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;

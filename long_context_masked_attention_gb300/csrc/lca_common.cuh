@@ -309,6 +309,18 @@ __device__ __forceinline__ uint32_t mask_bits(const MaskCtx& m, const SegInfo& s
     return span_bits(row_span(m, sg, i), j0);
   }
 }
+// mask_bits with the row's span computed once for all its tiles (the
+// interval families' span depends on the row alone).
+template <bool kCols>
+__device__ __forceinline__ uint32_t mask_bits_row(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0,
+                                                  const Span& row) {
+  if constexpr (kCols) {
+    return flashmask_chunk_bits(m, sg, i, j0);
+  } else {
+    if (is_block_sparse(m.kind)) return block_chunk_bits(m, sg, hm, i, j0);
+    return span_bits(row, j0);
+  }
+}
 // Any family, chosen at run time (planning and test kernels).
 __device__ __forceinline__ uint32_t mask_bits_any(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
   return (m.kind == kFlashMask) ? mask_bits<true>(m, sg, hm, i, j0) : mask_bits<false>(m, sg, hm, i, j0);

@@ -455,6 +455,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
     const SegInfo sg = pv.segs[inf.seg];
     const int i = inf.qb * 2 * kTile + x * kTile + row;  // row inside the segment
     const bool valid = i < sg.q_len;
+    const Span row_sp = row_span(pv.mask, sg, i);  // interval families: the row's keys, for every tile
     float m_use = -INFINITY, l = 0.f;
     bool any = false;
     uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
@@ -482,7 +483,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       }
       if (cls == kTilePartial && !blk) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mb[c] = mask_bits<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c);
+        for (int c = 0; c < 4; ++c) mb[c] = mask_bits_row<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c, row_sp);
       }
       if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
       ++s_cons;
