@@ -299,7 +299,7 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     const SegInfo sg = pv.segs[inf.seg];
     const int i = inf.qt * kTile + row;
     const bool valid = i < sg.q_len;
-    const Span row_sp = row_span(pv.mask, sg, i);  // interval families: the row's keys, for every tile
+    const Span row_sp = row_mask_ctx(pv.mask, sg, i);  // the row's span or query block, for every tile
     const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
     const uint64_t nl2 = f2(valid ? a.nlse2[stat] : -INFINITY, valid ? a.nlse2[stat] : -INFINITY);  // -LSE2, twice
     const float nDv = valid ? a.nD[stat] : 0.f;

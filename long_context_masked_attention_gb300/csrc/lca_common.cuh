@@ -242,11 +242,12 @@ __device__ __forceinline__ bool block_kept(const MaskCtx& m, int hm, int qb, int
   return (w >> (kb & 31)) & 1u;
 }
 
-// 32-column mask chunk for block-sparse maps.  A chunk touches at most two
-// key blocks because every key block but the last is at least 32 wide.
-__device__ __forceinline__ uint32_t block_chunk_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
+// 32-column mask chunk for block-sparse maps, row i being in query block
+// qb.  A chunk touches at most two key blocks because every key block but
+// the last is at least 32 wide.
+__device__ __forceinline__ uint32_t block_chunk_bits_q(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0,
+                                                       int qb) {
   if (i < 0 || i >= sg.q_len || j0 >= sg.k_len) return 0u;
-  const int qb = q_block_of(m, sg.q_off + i);
   const int jl = min(j0 + 31, sg.k_len - 1);
   const int gj0 = sg.k_off + j0;
   const int kA = k_block_of(m, gj0), kB = k_block_of(m, sg.k_off + jl);
@@ -261,6 +262,11 @@ __device__ __forceinline__ uint32_t block_chunk_bits(const MaskCtx& m, const Seg
     bits = (keepA ? low : 0u) | (keepB ? ~low : 0u);
   }
   return bits & range_bits(0, sg.k_len, j0);
+}
+
+__device__ __forceinline__ uint32_t block_chunk_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0) {
+  if (i < 0 || i >= sg.q_len || j0 >= sg.k_len) return 0u;
+  return block_chunk_bits_q(m, sg, hm, i, j0, q_block_of(m, sg.q_off + i));
 }
 
 // ---------------------------------------------------------------- FlashMask
@@ -309,15 +315,26 @@ __device__ __forceinline__ uint32_t mask_bits(const MaskCtx& m, const SegInfo& s
     return span_bits(row_span(m, sg, i), j0);
   }
 }
-// mask_bits with the row's span computed once for all its tiles (the
-// interval families' span depends on the row alone).
+// What a row's mask words need that does not change from tile to tile,
+// computed once per work item: the interval families' key span, or for a
+// block map the row's query block (carried in a0).
+__device__ __forceinline__ Span row_mask_ctx(const MaskCtx& m, const SegInfo& sg, int i) {
+  if (is_block_sparse(m.kind)) {
+    Span s{0, 0, 0, 0};
+    if (i >= 0 && i < sg.q_len) s.a0 = q_block_of(m, sg.q_off + i);
+    return s;
+  }
+  return row_span(m, sg, i);
+}
+
+// mask_bits from the row's context (row_mask_ctx).
 template <bool kCols>
 __device__ __forceinline__ uint32_t mask_bits_row(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0,
                                                   const Span& row) {
   if constexpr (kCols) {
     return flashmask_chunk_bits(m, sg, i, j0);
   } else {
-    if (is_block_sparse(m.kind)) return block_chunk_bits(m, sg, hm, i, j0);
+    if (is_block_sparse(m.kind)) return block_chunk_bits_q(m, sg, hm, i, j0, row.a0);
     return span_bits(row, j0);
   }
 }

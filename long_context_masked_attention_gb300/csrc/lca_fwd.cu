@@ -455,7 +455,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
     const SegInfo sg = pv.segs[inf.seg];
     const int i = inf.qb * 2 * kTile + x * kTile + row;  // row inside the segment
     const bool valid = i < sg.q_len;
-    const Span row_sp = row_span(pv.mask, sg, i);  // interval families: the row's keys, for every tile
+    const Span row_sp = row_mask_ctx(pv.mask, sg, i);  // the row's span or query block, for every tile
     float m_use = -INFINITY, l = 0.f;
     bool any = false;
     uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
