@@ -112,7 +112,8 @@ struct Layout {
   size_t f_cnt = 0, f_key = 0, f_order = 0, f_ent = 0;
   size_t D = 0, lse2 = 0, q_cnt = 0, q_key = 0, q_order = 0, q_ent = 0, k_ucost = 0, k_key = 0, k_order = 0,
          k_lcnt = 0, k_lsteps = 0, k_ent = 0;
-  size_t k_usteps = 0, k_nchunk = 0, k_istart = 0, k_sstart = 0, k_nwork = 0, k_part = 0, k_runfirst = 0, k_runof = 0;
+  size_t k_usteps = 0, k_nchunk = 0, k_istart = 0, k_sstart = 0, k_nwork = 0, k_part = 0, k_runfirst = 0, k_runof = 0,
+         k_runat = 0;
   int k_max_slots = 0;
   size_t total = 0;
 };
@@ -380,6 +381,7 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     L.k_nwork = take(2 * sizeof(int));
     L.k_runfirst = take(sizeof(int) * n_units);
     L.k_runof = take(sizeof(int) * n_units);
+    L.k_runat = take(sizeof(int) * n_units);
     // partial-sum slots for chunks of split dK/dV units: [slot][dV, dK][128][128] f32
     L.k_max_slots = static_cast<int>(std::min<size_t>(kMaxPartialSlots, 2 * n_units * (P.Hkv / hkv_m)));
     L.k_part = take(sizeof(float) * 2 * kTile * kHeadDim * static_cast<size_t>(L.k_max_slots));
@@ -951,6 +953,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     sp.max_slots = c.L.k_max_slots;
     sp.run_first = reinterpret_cast<int*>(c.ws + c.L.k_runfirst);
     sp.run_of = reinterpret_cast<int*>(c.ws + c.L.k_runof);
+    sp.run_at = reinterpret_cast<int*>(c.ws + c.L.k_runat);
     ph = phase_begin(3, sk);
     launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, sk);
     launch_sort(wl, sk);
@@ -973,6 +976,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.n_work_dev = sp.n_work;
     a.run_first = sp.run_first;
     a.run_of = sp.run_of;
+    a.run_at = sp.run_at;
     a.partials = reinterpret_cast<float*>(c.ws + c.L.k_part);
     a.n_units = static_cast<int>(k_units);
     a.nD = D;

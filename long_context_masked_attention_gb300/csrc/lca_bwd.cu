@@ -558,9 +558,10 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
           const int mid = (lo + hi) >> 1;
           if (a.item_start[mid] <= w) lo = mid; else hi = mid;
         }
-        // run `lo` holds item w; inside a run items go chunk, KV head, unit
-        const int first = a.run_first[lo];
-        const int n_r = ((lo + 1 < n_runs) ? a.run_first[lo + 1] : a.n_units) - first;
+        // claim position `lo` holds item w; inside its run items go chunk, KV head, unit
+        const int run = a.run_at[lo];
+        const int first = a.run_first[run];
+        const int n_r = ((run + 1 < n_runs) ? a.run_first[run + 1] : a.n_units) - first;
         const int local = w - a.item_start[lo];
         const int per_chunk = n_r * a.expand;
         const int c = local / per_chunk;
@@ -579,7 +580,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         const long long S = a.usteps[unit];
         inf.begin = static_cast<int>(S * c / P);
         inf.nsteps = static_cast<int>(S * (c + 1) / P) - inf.begin;
-        inf.slot = (P > 1) ? a.split_start[lo] + local : -1;
+        inf.slot = (P > 1) ? a.split_start[run] + local : -1;
       }
       if (lane == 0) {
         items[slot] = inf;

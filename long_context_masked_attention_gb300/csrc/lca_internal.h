@@ -78,11 +78,12 @@ void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl
 // count) with their item and partial-slot prefixes.
 struct DkvSplit {
   int* nchunk;       // per unit: chunks of each of its items (1 = whole)
-  int* item_start;   // per run: first work item (n_runs + 1 entries)
+  int* item_start;   // per claim position: first work item (n_runs + 1 entries)
   int* split_start;  // per run: first partial slot
   int* n_work;       // [0] work items, [1] runs
   int* run_first;    // per run: first sorted unit
   int* run_of;       // per sorted unit: its run
+  int* run_at;       // per claim position: its run (runs by descending item cost)
   int max_slots;
 };
 void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st);
@@ -122,13 +123,14 @@ struct AttnArgs {
   // dK/dV: units far longer than a share of the per-SM load, and the last
   // units of the cost order, are cut into chunks of 64-row steps; a chunk
   // writes f32 partial dV, dK that a reduction sums.
-  const int* item_start;   // [n_runs + 1] first work item of each run of sorted units
+  const int* item_start;   // [n_runs + 1] first work item of each claim position
   const int* split_start;  // [n_runs] first partial slot of each run
   const int* nchunk;       // [unit] chunks of each of the unit's items (1 = whole)
   const int* usteps;       // [unit] 64-row steps of each of the unit's items
   const int* n_work_dev;   // [0] work items, [1] runs, written on the device by the split pass
   const int* run_first;    // [n_runs] first sorted unit of each run
   const int* run_of;       // [n_units] run of each sorted unit
+  const int* run_at;       // [n_runs] run at each claim position
   float* partials;         // [slot][dV, dK][128 rows][128] f32
   int n_units;
   int* status;

@@ -305,8 +305,11 @@ void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl
 // units with the same cost bucket and chunk count.  Inside a run the items
 // go chunk by chunk, then KV head by KV head, then unit by unit, so that the
 // CTAs claiming consecutive items work on the same KV head's query rows at
-// the same time (they share Q and dO tiles in L2) while the order across
-// runs stays longest first.
+// the same time (they share Q and dO tiles in L2).  The runs are claimed in
+// descending order of their items' cost (a unit's cost over its chunk
+// count), so that the halves of the tail cut do not go before whole units
+// that are longer than they are (short key tiles at the end of a sliding
+// window stay whole while the equal tiles before them are halved).
 __device__ __forceinline__ long long block_sum_ll(long long v, long long* red) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
@@ -357,9 +360,11 @@ __global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__
                                                          int num_sms, int max_slots, int* __restrict__ nchunk,
                                                          int* __restrict__ item_start,
                                                          int* __restrict__ split_start, int* __restrict__ n_work,
-                                                         int* __restrict__ run_first, int* __restrict__ run_of) {
+                                                         int* __restrict__ run_first, int* __restrict__ run_of,
+                                                         int* __restrict__ run_at) {
   __shared__ long long red_ll[32];
   __shared__ int red[32];
+  __shared__ int bucket_pos[kCostBuckets];
   long long local = 0;
   for (int u = threadIdx.x; u < n_units; u += blockDim.x) local += ucost[u];
   const long long total = block_sum_ll(local, red_ll) * expand;
@@ -404,26 +409,68 @@ __global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__
   }
   const int n_runs = run_base;
   __syncthreads();
-  int item_base = 0, slot_base = 0;
+  // partial slots, in run order
+  int slot_base = 0;
   for (int r0 = 0; r0 < n_runs; r0 += blockDim.x) {
     const int r = r0 + threadIdx.x;
-    int ni = 0, si = 0;
+    int si = 0;
     if (r < n_runs) {
       const int first = run_first[r];
       const int last = (r + 1 < n_runs) ? run_first[r + 1] : n_units;
       const int c = nchunk[order[first]];
-      ni = c * expand * (last - first);
-      si = (c > 1) ? ni : 0;
+      si = (c > 1) ? c * expand * (last - first) : 0;
     }
-    int tot_i, tot_s;
-    const int pi = block_scan_excl(ni, red, tot_i);
+    int tot_s;
     const int ps = block_scan_excl(si, red, tot_s);
-    if (r < n_runs) {
-      item_start[r] = item_base + pi;
-      split_start[r] = slot_base + ps;
-    }
-    item_base += tot_i;
+    if (r < n_runs) split_start[r] = slot_base + ps;
     slot_base += tot_s;
+  }
+  // claim order: runs by descending item cost (a counting sort on the cost
+  // bucket; runs in one bucket take its positions in no particular order,
+  // which changes no result: a run's partial slots follow its run index),
+  // run_at[position] = run
+  for (int b = threadIdx.x; b < kCostBuckets; b += blockDim.x) bucket_pos[b] = 0;
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_runs; r += blockDim.x) {
+    const int u = order[run_first[r]];
+    atomicAdd(&bucket_pos[kCostBuckets - 1 - cost_bucket(ucost[u] / nchunk[u])], 1);
+  }
+  __syncthreads();
+  {
+    constexpr int kPer = kCostBuckets / 1024;  // buckets per thread
+    int v[kPer], sum = 0;
+    for (int j = 0; j < kPer; ++j) {
+      v[j] = bucket_pos[threadIdx.x * kPer + j];
+      sum += v[j];
+    }
+    int tot;
+    int pre = block_scan_excl(sum, red, tot);
+    for (int j = 0; j < kPer; ++j) {
+      bucket_pos[threadIdx.x * kPer + j] = pre;
+      pre += v[j];
+    }
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < n_runs; r += blockDim.x) {
+    const int u = order[run_first[r]];
+    run_at[atomicAdd(&bucket_pos[kCostBuckets - 1 - cost_bucket(ucost[u] / nchunk[u])], 1)] = r;
+  }
+  __syncthreads();
+  // first work item of each claim position
+  int item_base = 0;
+  for (int p0 = 0; p0 < n_runs; p0 += blockDim.x) {
+    const int p = p0 + threadIdx.x;
+    int ni = 0;
+    if (p < n_runs) {
+      const int r = run_at[p];
+      const int first = run_first[r];
+      const int last = (r + 1 < n_runs) ? run_first[r + 1] : n_units;
+      ni = nchunk[order[first]] * expand * (last - first);
+    }
+    int tot_i;
+    const int pi = block_scan_excl(ni, red, tot_i);
+    if (p < n_runs) item_start[p] = item_base + pi;
+    item_base += tot_i;
   }
   if (threadIdx.x == 0) {
     item_start[n_runs] = item_base;
@@ -436,7 +483,7 @@ void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp,
   note_launches(1);
   split_dkv_kernel<<<1, 1024, 0, st>>>(wl.order, wl.cnt, usteps, wl.key, wl.n_sorted, wl.expand, num_sms,
                                        sp.max_slots, sp.nchunk, sp.item_start, sp.split_start, sp.n_work,
-                                       sp.run_first, sp.run_of);
+                                       sp.run_first, sp.run_of, sp.run_at);
 }
 
 // ---------------------------------------------------------------- cost sort
