@@ -807,6 +807,10 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(n_rows * wl.expand);
+    // MHA with long segments: rows in groups, so that the items in flight
+    // share each head's K/V in L2 (with short segments the plain order's
+    // balance is worth more)
+    a.row_group = (P.Hq == P.Hkv && wl.expand > 1 && P.max_q_len >= kMhaLongSegment) ? kMhaRowGroup : 1;
     a.o = o;
     a.lse = lse;
     a.prof = prof_slot(0, c.st);

@@ -25,9 +25,12 @@ constexpr CostWeights kCostFwd{4, 10}, kCostDq{4, 5}, kCostDkv{4, 6};
 // load and an epilogue, worth about ten steps).
 constexpr int kMinChunkSteps = 64;
 // dQ items of MHA (every query head with its own K/V) run in groups of this
-// many sorted rows, head by head (measured: 32K causal MHA backward 12.5%
-// faster; the forward and GQA gain nothing, the forward loses balance).
+// many sorted rows, head by head (measured: causal MHA backward 4% faster at
+// 8K and 32K; GQA gains nothing).  The forward does the same only when a
+// segment is at least kMhaLongSegment tokens long: at 32K the L2 reuse won
+// 10%, at 8K the lost balance cost 5-20%.
 constexpr int kMhaRowGroup = 8;
+constexpr int kMhaLongSegment = 16384;
 
 // Counts kernel launches made by this library (see lca_launch_count).
 void note_launches(int n);
