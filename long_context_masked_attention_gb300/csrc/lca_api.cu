@@ -92,6 +92,7 @@ struct HostPlan {
   int R256 = 0, R128 = 0, RK = 0;
   long long fwd_per_hm = 0, dq_per_hm = 0, dkv_per_hm = 0;
   int max_q_len = 0;
+  bool fwd_pair = false;  // forward items pair two query heads (see validate)
   std::vector<std::pair<int, int>> q_gaps, k_gaps;  // [start, len)
   // mask parameters
   MaskCtx mask{};
@@ -308,6 +309,27 @@ lca_status validate(const lca_shape* sh, const lca_mask_desc* md, HostPlan& P) {
     default:
       break;
   }
+  // Forward items of 128 rows of two query heads (which read the same KV
+  // head and the same mask map) instead of 256 rows of one head, for the
+  // families whose rows see few key tiles or tile ranges that shift row by
+  // row: the two sub-tiles then share one key-tile list and never wait on
+  // each other (measured: 8K windowed and document masks faster in the
+  // forward; FULL, CAUSAL and PREFIX_LM_CAUSAL keep 256-row items).
+  switch (P.kind) {
+    case LCA_MASK_SLIDING:
+    case LCA_MASK_CAUSAL_SLIDING:
+    case LCA_MASK_GLOBAL_SLIDING:
+    case LCA_MASK_DOC:
+    case LCA_MASK_CAUSAL_DOC:
+    case LCA_MASK_SHARED_QUESTION:
+    case LCA_MASK_CAUSAL_BLOCKWISE:
+    case LCA_MASK_PREFIX_LM_DOC:
+    case LCA_MASK_BLOCK_CAUSAL_DOC:
+      P.fwd_pair = P.hm_count == 1 && P.G % 2 == 0;
+      break;
+    default:
+      P.fwd_pair = false;
+  }
   return LCA_OK;
 }
 
@@ -354,10 +376,12 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
   const size_t H = static_cast<size_t>(P.hm_count);
   L.tcls = take(std::max<size_t>(1, H * P.dq_per_hm));
   if (fwd) {
-    L.f_cnt = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
-    L.f_key = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
-    L.f_order = take(sizeof(int) * std::max<size_t>(1, H * P.R256));
-    L.f_ent = take(sizeof(uint32_t) * std::max<size_t>(1, H * P.fwd_per_hm));
+    const size_t f_rows = P.fwd_pair ? P.R128 : P.R256;
+    const size_t f_ents = static_cast<size_t>(P.fwd_pair ? P.dq_per_hm : P.fwd_per_hm);
+    L.f_cnt = take(sizeof(int) * std::max<size_t>(1, H * f_rows));
+    L.f_key = take(sizeof(int) * std::max<size_t>(1, H * f_rows));
+    L.f_order = take(sizeof(int) * std::max<size_t>(1, H * f_rows));
+    L.f_ent = take(sizeof(uint32_t) * std::max<size_t>(1, H * f_ents));
   }
   if (bwd) {
     const size_t hkv_m = (P.hm_count == 1) ? 1 : static_cast<size_t>(P.Hkv);
@@ -773,7 +797,7 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
   }
   if (P.Tk > 0 && (!device_input(k) || !device_input(v))) return LCA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LCA_ERR_INVALID_ARG;
-  const long long n_rows = static_cast<long long>(P.hm_count) * P.R256;
+  const long long n_rows = static_cast<long long>(P.hm_count) * (P.fwd_pair ? P.R128 : P.R256);
   CUtensorMap tq, tk, tv;
   if (n_rows > 0) {
     if (!make_map(&tq, q, P.Tq, P.Hq, kTile) || !make_map(&tk, k, P.Tk, P.Hkv, kTile) ||
@@ -793,11 +817,11 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     wl.hist = reinterpret_cast<uint32_t*>(c.ws + c.L.hist);
     wl.counter = reinterpret_cast<int*>(c.ws + c.L.counters);
     wl.n_sorted = static_cast<int>(n_rows);
-    wl.expand = P.Hq / P.hm_count;
+    wl.expand = P.Hq / P.hm_count / (P.fwd_pair ? 2 : 1);  // heads (or head pairs) per list row
     int ph = phase_begin(0, c.st);
     uint8_t* tcls = c.ws + c.L.tcls;
     launch_classify(c.V, tcls, c.st);
-    launch_plan_fwd(c.V, tcls, wl, c.st);
+    launch_plan_fwd(c.V, tcls, wl, P.fwd_pair, c.st);
     launch_sort(wl, c.st);
     phase_end(ph, c.st);
     AttnArgs a = base_args(c, dr);
@@ -811,6 +835,7 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     // share each head's K/V in L2 (with short segments the plain order's
     // balance is worth more)
     a.row_group = (P.Hq == P.Hkv && wl.expand > 1 && P.max_q_len >= kMhaLongSegment) ? kMhaRowGroup : 1;
+    a.fwd_pair = P.fwd_pair ? 1 : 0;
     a.o = o;
     a.lse = lse;
     a.prof = prof_slot(0, c.st);

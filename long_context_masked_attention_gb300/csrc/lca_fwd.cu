@@ -113,16 +113,20 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       if (w < a.n_work) {
         int sorted_row, head;
         item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
+        // an item is 256 rows of one head, or (paired) 128 rows of two heads
         const int row = a.order[sorted_row];
-        const int hm = row / pv.R256, rr = row % pv.R256;
-        const int s = find_bucket(pv.q256_start, pv.n_seg, rr);
+        const int R = a.fwd_pair ? pv.R128 : pv.R256;
+        const int* qstart = a.fwd_pair ? pv.q128_start : pv.q256_start;
+        const int hm = row / R, rr = row % R;
+        const int s = find_bucket(qstart, pv.n_seg, rr);
         inf.valid = 1;
         inf.seg = s;
-        inf.qb = rr - pv.q256_start[s];
+        inf.qb = rr - qstart[s];
         inf.hm = hm;
-        inf.head = (pv.hm_count == 1) ? head : hm;
+        inf.head = (pv.hm_count == 1) ? (a.fwd_pair ? 2 * head : head) : hm;
         inf.cnt = a.cnt[row];
-        inf.ebase = hm * pv.fwd_per_hm + pv.fwd_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk;
+        inf.ebase = a.fwd_pair ? hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk
+                               : hm * pv.fwd_per_hm + pv.fwd_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk;
       }
       items[slot] = inf;
       mbar_arrive(&bar[B_ITFULL + slot]);
@@ -137,13 +141,13 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       const SegInfo sg = pv.segs[inf.seg];
       if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 11)) goto abort;
       mbar_arrive_expect_tx(&bar[B_QFULL], 2 * kTileBytes);
-      const int y0 = sg.q_off + inf.qb * 2 * kTile;
+      const int y0 = sg.q_off + inf.qb * (a.fwd_pair ? 1 : 2) * kTile;
 #pragma unroll
       for (int x = 0; x < 2; ++x)
 #pragma unroll
         for (int c = 0; c < 2; ++c)
-          tma_load_2d(sQ + x * kTileBytes + c * kChunkBytes, tq, &bar[B_QFULL], inf.head * kHeadDim + c * 64,
-                      y0 + x * kTile);
+          tma_load_2d(sQ + x * kTileBytes + c * kChunkBytes, tq, &bar[B_QFULL],
+                      (inf.head + (a.fwd_pair ? x : 0)) * kHeadDim + c * 64, y0 + (a.fwd_pair ? 0 : x * kTile));
       q_issued = it + 1;
 
       const int g = inf.head / pv.G;
@@ -453,7 +457,9 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
     if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
     if (!inf.valid) return;
     const SegInfo sg = pv.segs[inf.seg];
-    const int i = inf.qb * 2 * kTile + x * kTile + row;  // row inside the segment
+    // row inside the segment and query head of this sub-tile
+    const int i = a.fwd_pair ? inf.qb * kTile + row : inf.qb * 2 * kTile + x * kTile + row;
+    const int head = inf.head + (a.fwd_pair ? x : 0);
     const bool valid = i < sg.q_len;
     const Span row_sp = row_mask_ctx(pv.mask, sg, i);  // the row's span or query block, for every tile
     float m_use = -INFINITY, l = 0.f;
@@ -508,8 +514,8 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       if (blk)
         sum = tile_exp_blk(tS, keep4, sl2, base);
       else
-        sum = (cls == kTilePartial) ? tile_exp<true, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0)
-                                    : tile_exp<false, kDrop>(tS, mb, sl2, base, a, dc, grow, inf.head, g0);
+        sum = (cls == kTilePartial) ? tile_exp<true, kDrop>(tS, mb, sl2, base, a, dc, grow, head, g0)
+                                    : tile_exp<false, kDrop>(tS, mb, sl2, base, a, dc, grow, head, g0);
       l = l * factor + sum;
       if (__any_sync(0xFFFFFFFFu, need)) {
         // the previous O_x += P_x V must have finished before O_x is rescaled
@@ -533,7 +539,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       any = true;
     }
     // epilogue: O = O / l (bf16), LSE = (m + log2 l) ln 2
-    __nv_bfloat16* orow = O + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + inf.head) * kHeadDim;
+    __nv_bfloat16* orow = O + (static_cast<size_t>(sg.q_off + (valid ? i : 0)) * pv.Hq + head) * kHeadDim;
     if (any) {
       if (!waitw(&bar[B_OFULL + x], (p_prod - 1) & 1, a, 36 + x)) return;
       tc_fence_after();
@@ -561,7 +567,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       for (int u = 0; u < 16; ++u) *reinterpret_cast<uint4*>(orow + 8 * u) = make_uint4(0, 0, 0, 0);
     }
     if (valid) {
-      a.lse[static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i] =
+      a.lse[static_cast<size_t>(head) * pv.Tq + sg.q_off + i] =
           (l > 0.f) ? (m_use + log2f(l)) * kLn2 : -INFINITY;
     }
     tc_fence_before();

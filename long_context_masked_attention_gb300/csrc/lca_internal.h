@@ -72,7 +72,10 @@ void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int
                              size_t keep_bytes, int* status, cudaStream_t st);
 // Class of every 128x128 tile, [map head][segment at dq_off][query tile][key tile] bytes.
 void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st);
-void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st);
+// Forward lists: one row per 256 query rows (two 128-row sub-tiles), or with
+// `pair` one row per 128 query rows whose class serves both sub-tiles (two
+// query heads of one KV head and one mask map).
+void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, bool pair, cudaStream_t st);
 void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st);
 void launch_plan_dkv(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, int* list_cnt, int* list_steps,
                      int* usteps, cudaStream_t st);
@@ -123,6 +126,7 @@ struct AttnArgs {
   int n_work;
   int expand;
   int row_group;  // forward, dQ: sorted rows per group of the item order (see item_of)
+  int fwd_pair;   // forward: items are 128 rows of two query heads (1) or 256 rows of one (0)
   // dK/dV: units far longer than a share of the per-SM load, and the last
   // units of the cost order, are cut into chunks of 64-row steps; a chunk
   // writes f32 partial dV, dK that a reduction sums.

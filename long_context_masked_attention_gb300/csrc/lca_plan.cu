@@ -155,7 +155,8 @@ __device__ __forceinline__ int cost_bucket(long long c) {
 // One warp per list row (map head, segment, query block of SUB*128 rows); the
 // warp takes 32 key tiles at a time and places the non-empty ones with a ballot.
 // Entry = key tile index | class of sub-tile 0 << 24 | class of sub-tile 1 << 26.
-// cnt = entries of the row, key = its cost bucket.
+// SUB = 3: rows of 128 queries whose class serves both sub-tiles (the
+// forward's paired heads).  cnt = entries of the row, key = its cost bucket.
 template <int SUB>
 __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls, int* __restrict__ cnt,
                                    int* __restrict__ key, uint32_t* __restrict__ entries,
@@ -173,7 +174,8 @@ __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls
   const long long per_hm = (SUB == 2) ? pv.fwd_per_hm : pv.dq_per_hm;
   const long long off = (SUB == 2) ? pv.fwd_off[s] : pv.dq_off[s];
   uint32_t* out = entries + hm * per_hm + off + static_cast<long long>(qb) * sg.nk;
-  const uint8_t* cls0 = tcls + hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(qb * SUB) * sg.nk;
+  const uint8_t* cls0 =
+      tcls + hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(qb * (SUB == 2 ? 2 : 1)) * sg.nk;
   const bool has1 = (SUB == 2) && (qb * SUB + 1 < nq);
   int n = 0, cost = 0;
   for (int k0 = 0; k0 < sg.nk; k0 += 32) {
@@ -182,6 +184,7 @@ __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls
     if (kt < sg.nk) {
       c0 = cls0[kt] & 3u;  // the half-empty flags serve the 64-row dK/dV steps only
       if (has1) c1 = cls0[sg.nk + kt] & 3u;
+      if (SUB == 3) c1 = c0;
     }
     const uint32_t keep = __ballot_sync(0xFFFFFFFFu, (c0 | c1) != 0);
     if ((c0 | c1) != 0) out[n + __popc(keep & ((1u << lane) - 1u))] = static_cast<uint32_t>(kt) | (c0 << 24) | (c1 << 26);
@@ -196,12 +199,16 @@ __global__ void plan_q_rows_kernel(PlanView pv, const uint8_t* __restrict__ tcls
   }
 }
 
-void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st) {
-  const int rows = pv.hm_count * pv.R256;
+void launch_plan_fwd(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, bool pair, cudaStream_t st) {
+  const int rows = pv.hm_count * (pair ? pv.R128 : pv.R256);
   if (rows == 0) return;
   note_launches(1);
-  plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, wl.key,
-                                                        static_cast<uint32_t*>(wl.entries), wl.hist, kCostFwd);
+  if (pair)
+    plan_q_rows_kernel<3><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, wl.key,
+                                                          static_cast<uint32_t*>(wl.entries), wl.hist, kCostFwd);
+  else
+    plan_q_rows_kernel<2><<<(rows + 7) / 8, 256, 0, st>>>(pv, tcls, wl.cnt, wl.key,
+                                                          static_cast<uint32_t*>(wl.entries), wl.hist, kCostFwd);
 }
 
 void launch_plan_dq(const PlanView& pv, const uint8_t* tcls, const WorkList& wl, cudaStream_t st) {

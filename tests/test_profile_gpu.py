@@ -19,6 +19,17 @@ pytestmark = pytest.mark.gpu
 PROBS = [p for p in cases.gpu_small_all() if p.name in ("g_tiny_sliding_700", "g_tiny_causal_doc_docs", "g_small_bsu64")]
 
 
+# Families whose forward items pair two query heads of one KV head (128 rows
+# each) instead of taking 256 rows of one head, when G is even and the mask
+# map is shared by all heads.
+PAIRED = {"SLIDING", "CAUSAL_SLIDING", "GLOBAL_SLIDING", "DOC", "CAUSAL_DOC", "SHARED_QUESTION",
+          "CAUSAL_BLOCKWISE", "PREFIX_LM_DOC", "BLOCK_CAUSAL_DOC"}
+
+
+def _fwd_paired(prob):
+    return prob.mask.kind in PAIRED and (prob.Hq // prob.Hkv) % 2 == 0
+
+
 def _expected(lca, prob):
     call = lca.marshal(prob.Tq, prob.Tk, prob.Hq, prob.Hkv, prob.d, prob.segments, prob.mask, prob.scale)
     full = part = steps_full = steps_part = 0
@@ -37,7 +48,10 @@ def _expected(lca, prob):
                 steps_full += halves_in * int((c[qt] == 1).sum())
                 for b in cls[qt][c[qt] == 2]:
                     steps_part += int(not (b & 4)) + int(halves_in == 2 and not (b & 8))
-            fwd_items += -(-seg.q_len // 256)
+            if not _fwd_paired(prob):
+                fwd_items += -(-seg.q_len // 256)
+            elif h % 2 == 0:  # one item per 128 rows of a head pair
+                fwd_items += -(-seg.q_len // 128)
             dq_items += nq
     return dict(full=full, part=part, steps_full=steps_full, steps_part=steps_part, fwd_items=fwd_items,
                 dq_items=dq_items)
