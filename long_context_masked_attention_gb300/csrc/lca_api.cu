@@ -108,7 +108,7 @@ struct Layout {
   // blob-relative offsets
   size_t b_segs = 0, b_q256 = 0, b_q128 = 0, b_fwdoff = 0, b_dqoff = 0, b_kgs = 0, b_kgsegs = 0, b_kt = 0,
          b_parts = 0, b_qbb = 0, b_kbb = 0;
-  size_t keep = 0, keep_bytes = 0, qb_of = 0, kb_of = 0;
+  size_t keep = 0, keep_bytes = 0, qb_of = 0, kb_of = 0, vchunk = 0;
   size_t tcls = 0;
   size_t f_cnt = 0, f_key = 0, f_order = 0, f_ent = 0;
   size_t D = 0, lse2 = 0, q_cnt = 0, q_key = 0, q_order = 0, q_ent = 0, k_ucost = 0, k_key = 0, k_order = 0,
@@ -371,6 +371,8 @@ Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
     if (P.kind == kBlockSparseVariable) {
       L.qb_of = take(sizeof(int) * std::max(1, P.Tq));
       L.kb_of = take(sizeof(int) * std::max(1, P.Tk));
+      L.vchunk =
+          take(sizeof(uint32_t) * std::max<size_t>(1, static_cast<size_t>(P.mask.hm_count) * P.mask.n_qb * P.RK));
     }
   }
   const size_t H = static_cast<size_t>(P.hm_count);
@@ -445,6 +447,9 @@ PlanView make_view(const HostPlan& P, const Layout& L, uint8_t* ws) {
       v.mask.kb_of = reinterpret_cast<const int*>(ws + L.kb_of);
       v.mask.kb_start = reinterpret_cast<const int*>(blob + L.b_kbb);
       v.mask.qb_start = reinterpret_cast<const int*>(blob + L.b_qbb);
+      v.mask.vchunk = reinterpret_cast<const uint32_t*>(ws + L.vchunk);
+      v.mask.vkt = reinterpret_cast<const int*>(blob + L.b_kt);
+      v.mask.vrk = P.RK;
     }
   }
   v.segs = reinterpret_cast<const SegInfo*>(blob + L.b_segs);
@@ -646,6 +651,8 @@ lca_status upload(Call& c) {
                             reinterpret_cast<uint32_t*>(c.ws + c.L.keep), reinterpret_cast<int*>(c.ws + c.L.qb_of),
                             reinterpret_cast<int*>(c.ws + c.L.kb_of), c.P.blk_row_ptr, c.P.blk_col_idx, c.P.blk_nnz,
                             c.L.keep_bytes, reinterpret_cast<int*>(c.ws + c.L.status), c.st);
+    if (c.P.kind == kBlockSparseVariable)
+      launch_build_vchunk(c.V, reinterpret_cast<uint32_t*>(c.ws + c.L.vchunk), c.st);
   }
   LCA_CUDA(cudaGetLastError());
   return LCA_OK;

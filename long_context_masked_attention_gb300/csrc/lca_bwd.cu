@@ -354,11 +354,12 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         }
       }
       if (cls == kTilePartial) {
+        const uint32_t vw = blk ? 0u : row_tile_word(pv.mask, sg, inf.hm, i, kt, row_sp);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const uint32_t bits = blk ? (((keep2 >> c) & 1u) ? ~0u : 0u)
                                     : mask_bits_row<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + half * 64 + 32 * c,
-                                                           row_sp);
+                                                           row_sp, vw);
           if (!__all_sync(0xFFFFFFFFu, bits == ~0u)) {  // the warp's 32 rows do not all keep the chunk
 #pragma unroll
             for (int k = 0; k < 32; ++k) s[32 * c + k] = ((bits >> k) & 1u) ? s[32 * c + k] : -INFINITY;

@@ -79,6 +79,12 @@ struct MaskCtx {
   // every 32 rows x 32 keys of a tile (a warp's rows, a 32-column chunk)
   // then lie in one (query block, key block) pair
   int aligned;
+  // variable block map: per (map head, query block, key-group key tile) one
+  // word of four chunk bytes (see vchunk_bits); vkt = first key tile of each
+  // key group in that numbering, vrk = key tiles over all groups
+  const uint32_t* vchunk;
+  const int* vkt;
+  int vrk;
 };
 
 // Mask forms the attention kernels are compiled for: the interval families
@@ -315,6 +321,34 @@ __device__ __forceinline__ uint32_t mask_bits(const MaskCtx& m, const SegInfo& s
     return span_bits(row_span(m, sg, i), j0);
   }
 }
+// Variable block maps.  The chunk byte of 32 keys starting at j0 for query
+// block qb: bit 7 = the chunk's first key block is kept, bit 6 = its second
+// one (if it has one) is kept, bits 0-5 = the number of its keys in the first
+// block (32 when it lies in one block and inside its key group), or 63 when
+// the chunk crosses both a block bound and the group's last key (the mask
+// word is then evaluated per row).
+__device__ __forceinline__ uint32_t vchunk_byte(const MaskCtx& m, int hm, int qb, int g0, int k_end) {
+  if (g0 >= k_end) return 0u;
+  const int gl = min(g0 + 31, k_end - 1);
+  const int kA = m.kb_of[g0], kB = m.kb_of[gl];
+  const uint32_t keepA = block_kept(m, hm, qb, kA) ? 128u : 0u;
+  if (kA == kB) return keepA | static_cast<uint32_t>(gl - g0 + 1);
+  if (gl != g0 + 31) return 63u;
+  const uint32_t keepB = block_kept(m, hm, qb, kB) ? 64u : 0u;
+  return keepA | keepB | static_cast<uint32_t>(m.kb_start[kB] - g0);
+}
+
+// Mask word of row i for the chunk at j0 from the row's tile word vw.
+__device__ __forceinline__ uint32_t vchunk_bits(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0, int qb,
+                                                uint32_t vw) {
+  if (i < 0 || i >= sg.q_len || j0 >= sg.k_len) return 0u;
+  const uint32_t c8 = (vw >> (8 * ((j0 >> 5) & 3))) & 0xFFu;
+  const uint32_t split = c8 & 63u;
+  if (split == 63u) return block_chunk_bits_q(m, sg, hm, i, j0, qb);
+  const uint32_t low = split >= 32u ? ~0u : (1u << split) - 1u;
+  return (((c8 & 128u) ? low : 0u) | ((c8 & 64u) ? ~low : 0u)) & range_bits(0, sg.k_len, j0);
+}
+
 // What a row's mask words need that does not change from tile to tile,
 // computed once per work item: the interval families' key span, or for a
 // block map the row's query block (carried in a0).
@@ -327,13 +361,23 @@ __device__ __forceinline__ Span row_mask_ctx(const MaskCtx& m, const SegInfo& sg
   return row_span(m, sg, i);
 }
 
-// mask_bits from the row's context (row_mask_ctx).
+// The row's tile word for key tile kt of its segment (variable block maps;
+// 0 otherwise): one load per row and tile instead of the block lookups of
+// every chunk.
+__device__ __forceinline__ uint32_t row_tile_word(const MaskCtx& m, const SegInfo& sg, int hm, int i, int kt,
+                                                  const Span& row) {
+  if (m.kind != kBlockSparseVariable || i < 0 || i >= sg.q_len) return 0u;
+  return m.vchunk[(static_cast<size_t>(hm) * m.n_qb + row.a0) * m.vrk + m.vkt[sg.kg] + kt];
+}
+
+// mask_bits from the row's context (row_mask_ctx) and tile word (row_tile_word).
 template <bool kCols>
 __device__ __forceinline__ uint32_t mask_bits_row(const MaskCtx& m, const SegInfo& sg, int hm, int i, int j0,
-                                                  const Span& row) {
+                                                  const Span& row, uint32_t vw) {
   if constexpr (kCols) {
     return flashmask_chunk_bits(m, sg, i, j0);
   } else {
+    if (m.kind == kBlockSparseVariable) return vchunk_bits(m, sg, hm, i, j0, row.a0, vw);
     if (is_block_sparse(m.kind)) return block_chunk_bits_q(m, sg, hm, i, j0, row.a0);
     return span_bits(row, j0);
   }

@@ -488,8 +488,10 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
         }
       }
       if (cls == kTilePartial && !blk) {
+        const uint32_t vw = row_tile_word(pv.mask, sg, inf.hm, i, kt, row_sp);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mb[c] = mask_bits_row<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c, row_sp);
+        for (int c = 0; c < 4; ++c)
+          mb[c] = mask_bits_row<kCols>(pv.mask, sg, inf.hm, i, kt * kTile + 32 * c, row_sp, vw);
       }
       if (!waitw(&bar[B_SFULL + x], s_cons & 1, a, 32 + x)) return;
       ++s_cons;

@@ -70,6 +70,9 @@ struct WorkList {
 void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int* kb_bounds, uint32_t* keep,
                              int* qb_of, int* kb_of, const int* row_ptr, const int* col_idx, long long blk_nnz,
                              size_t keep_bytes, int* status, cudaStream_t st);
+// Variable block maps: the chunk words of every (map head, query block,
+// key-group key tile), [hm][n_qb][RK] (see vchunk_byte).
+void launch_build_vchunk(const PlanView& pv, uint32_t* out, cudaStream_t st);
 // Class of every 128x128 tile, [map head][segment at dq_off][query tile][key tile] bytes.
 void launch_classify(const PlanView& pv, uint8_t* tcls, cudaStream_t st);
 // Forward lists: one row per 256 query rows (two 128-row sub-tiles), or with

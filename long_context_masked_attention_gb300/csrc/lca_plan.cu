@@ -67,6 +67,31 @@ void launch_build_block_maps(const PlanView& pv, const int* qb_bounds, const int
   }
 }
 
+// ---------------------------------------------------------------- variable-map chunk words
+__global__ void build_vchunk_kernel(PlanView pv, uint32_t* __restrict__ out, long long total) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long w = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; w < total; w += stride) {
+    const int rk = static_cast<int>(w % pv.RK);
+    const long long r = w / pv.RK;
+    const int qb = static_cast<int>(r % pv.mask.n_qb), hm = static_cast<int>(r / pv.mask.n_qb);
+    const int kg = find_bucket(pv.kt_start, pv.n_kg, rk);
+    const KeyGroup grp = pv.kgs[kg];
+    const int g0 = grp.k_off + (rk - pv.kt_start[kg]) * kTile, k_end = grp.k_off + grp.k_len;
+    uint32_t word = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) word |= vchunk_byte(pv.mask, hm, qb, g0 + 32 * c, k_end) << (8 * c);
+    out[w] = word;
+  }
+}
+
+void launch_build_vchunk(const PlanView& pv, uint32_t* out, cudaStream_t st) {
+  const long long total = static_cast<long long>(pv.hm_count) * pv.mask.n_qb * pv.RK;
+  if (total == 0) return;
+  note_launches(1);
+  const long long blocks = std::min<long long>((total + 255) / 256, 1 << 20);
+  build_vchunk_kernel<<<static_cast<int>(blocks), 256, 0, st>>>(pv, out, total);
+}
+
 // ---------------------------------------------------------------- tile classes
 // Every 128x128 tile (query tile qt, key tile kt) of every segment and map
 // head is classified once, one warp per tile, into a byte array laid out like

@@ -310,3 +310,32 @@ def test_aligned_block_map_matches_variable_form(lca):
         g2 = run_bwd(lca, var, q, k, v, do, o1, l1)
         for name, x, y in zip(("dq", "dk", "dv"), g1, g2):
             assert np.array_equal(to_np(x), to_np(y)), (prob.name, name)
+
+
+def _variable_block_cases():
+    """Variable block maps over several segments: packed documents (one key
+    group each), and two query segments reading one key range (one key group
+    with two members), with ragged ends."""
+    from gen import MaskSpec, Problem, Segment, variable_block_bounds, variable_block_map
+
+    r = np.random.Generator(np.random.PCG64(81))
+    out = []
+    for T, segs, name in [
+        (1033, [(0, 400, 0, 400), (400, 300, 400, 300), (700, 333, 700, 333)], "docs"),
+        (1000, [(0, 260, 0, 700), (260, 440, 0, 700), (700, 300, 700, 300)], "shared_keys"),
+    ]:
+        qb = variable_block_bounds(T, 32, 256, r)
+        kb = variable_block_bounds(T, 32, 256, r)
+        rp, ci = variable_block_map(len(qb) - 1, len(kb) - 1, 4, r)
+        spec = MaskSpec("BLOCK_SPARSE_VARIABLE", qb_bounds=qb, kb_bounds=kb, heads_in_map=4, blk_row_ptr=rp,
+                        blk_col_idx=ci)
+        out.append(Problem("variable_" + name, T, T, 4, 2, 128, [Segment(*s) for s in segs], spec, 82))
+    return out
+
+
+VARIABLE = _variable_block_cases()
+
+
+@pytest.mark.parametrize("prob", VARIABLE, ids=[p.name for p in VARIABLE])
+def test_variable_block_map_segments_parity(lca, prob):
+    _parity(lca, prob)
