@@ -48,10 +48,13 @@ def test_flashmask_attention_parity_and_same_as_family(lca, prob):
         assert np.array_equal(to_np(a), to_np(b))
 
 
-@pytest.mark.parametrize("kind", ["CAUSAL", "SHARED_QUESTION"])
+@pytest.mark.parametrize("kind", ["CAUSAL", "SHARED_QUESTION", "SLIDING", "GLOBAL_SLIDING", "CAUSAL_DOC"])
 def test_flashmask_8k_full_size(lca, kind):
     """Full-size masks bit-exact on the first and last heads' segment, and the
-    outputs equal to the family descriptor's."""
+    outputs equal to the family descriptor's.  The windowed and document
+    families run the forward with paired query heads (two heads of one KV
+    head per item) and the column descriptor with one head per item, so the
+    equality also checks the pairing."""
     prob = config2(kind)
     fm = as_flashmask(prob)
     _check_masks(lca, fm, [0])
