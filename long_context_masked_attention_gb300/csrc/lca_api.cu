@@ -838,10 +838,10 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(n_rows * wl.expand);
-    // MHA with long segments: rows in groups, so that the items in flight
-    // share each head's K/V in L2 (with short segments the plain order's
-    // balance is worth more)
-    a.row_group = (P.Hq == P.Hkv && wl.expand > 1 && P.max_q_len >= kMhaLongSegment) ? kMhaRowGroup : 1;
+    // MHA with segments of 8K rows or more on average: segment by segment,
+    // head by head (shorter segments keep the cost order, whose balance is
+    // worth more there: 2K and document batches were 10-13 % slower)
+    a.row_group = (P.Hq == P.Hkv && wl.expand > 1 && P.Tq >= 8192LL * std::max(1, P.n_seg)) ? -1 : 1;
     a.fwd_pair = P.fwd_pair ? 1 : 0;
     a.o = o;
     a.lse = lse;
@@ -1048,7 +1048,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(q_rows * wl.expand);
-    a.row_group = (P.Hq == P.Hkv && wl.expand > 1) ? kMhaRowGroup : 1;
+    a.row_group = (P.Hq == P.Hkv && wl.expand > 1) ? -1 : 1;  // MHA: segment by segment, head by head
     a.nD = D;
     a.nlse2 = lse2;
     a.dq = dq;

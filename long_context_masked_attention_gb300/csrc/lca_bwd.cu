@@ -107,9 +107,14 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       Item inf;
       inf.valid = 0;
       if (w < a.n_work) {
-        int sorted_row, head;
-        item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
-        const int row = a.order[sorted_row];
+        int row, head;
+        if (a.row_group < 0) {
+          seg_major_item(w, pv.q128_start, pv.n_seg, a.expand, row, head);
+        } else {
+          int sorted_row;
+          item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
+          row = a.order[sorted_row];
+        }
         const int hm = row / pv.R128, rr = row % pv.R128;
         const int s = find_bucket(pv.q128_start, pv.n_seg, rr);
         inf.valid = 1;

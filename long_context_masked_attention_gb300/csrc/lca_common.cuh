@@ -233,6 +233,19 @@ __device__ __forceinline__ void item_of(int w, int rows, int expand, int group, 
   row = base + local % n;
 }
 
+// Work item w of a query-major list with one mask map, taken segment by
+// segment, head by head, and within a head the segment's rows from last to
+// first (the longest first for causal rows): the items in flight then cover
+// a few heads of one segment, whose K/V stays in L2 when every head has its
+// own K/V.  qstart = row prefix over segments; row is the list row.
+__device__ __forceinline__ void seg_major_item(int w, const int* qstart, int n_seg, int expand, int& row, int& head) {
+  const int s = find_bucket(qstart, n_seg, w / expand);
+  const int rows_s = qstart[s + 1] - qstart[s];
+  const int local = w - qstart[s] * expand;
+  head = local / rows_s;
+  row = qstart[s] + rows_s - 1 - local % rows_s;
+}
+
 // ---------------------------------------------------------------- block-sparse
 __device__ __forceinline__ int q_block_of(const MaskCtx& m, int gq) {
   return (m.kind == kBlockSparseUniform) ? gq / m.q_block : m.qb_of[gq];

@@ -111,12 +111,17 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       Item inf;
       inf.valid = 0;
       if (w < a.n_work) {
-        int sorted_row, head;
-        item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
         // an item is 256 rows of one head, or (paired) 128 rows of two heads
-        const int row = a.order[sorted_row];
         const int R = a.fwd_pair ? pv.R128 : pv.R256;
         const int* qstart = a.fwd_pair ? pv.q128_start : pv.q256_start;
+        int row, head;
+        if (a.row_group < 0) {
+          seg_major_item(w, qstart, pv.n_seg, a.expand, row, head);
+        } else {
+          int sorted_row;
+          item_of(w, a.n_work / a.expand, a.expand, a.row_group, sorted_row, head);
+          row = a.order[sorted_row];
+        }
         const int hm = row / R, rr = row % R;
         const int s = find_bucket(qstart, pv.n_seg, rr);
         inf.valid = 1;

@@ -24,13 +24,11 @@ constexpr CostWeights kCostFwd{4, 10}, kCostDq{4, 5}, kCostDkv{4, 6};
 // A dK/dV chunk is at least this many 64-row steps long (a chunk pays a K/V
 // load and an epilogue, worth about ten steps).
 constexpr int kMinChunkSteps = 64;
-// dQ items of MHA (every query head with its own K/V) run in groups of this
-// many sorted rows, head by head (measured: causal MHA backward 4% faster at
-// 8K and 32K; GQA gains nothing).  The forward does the same only when a
-// segment is at least kMhaLongSegment tokens long: at 32K the L2 reuse won
-// 10%, at 8K the lost balance cost 5-20%.
-constexpr int kMhaRowGroup = 8;
-constexpr int kMhaLongSegment = 16384;
+// With every query head on its own K/V (MHA) and one mask map, dQ items (and
+// forward items when the segments average 8K rows or more) go segment by
+// segment and head by head (seg_major_item), so the items in flight share
+// K/V in L2 instead of streaming every head's K/V from HBM (8K causal MHA:
+// forward and backward 10 % faster).
 
 // Counts kernel launches made by this library (see lca_launch_count).
 void note_launches(int n);
@@ -128,7 +126,7 @@ struct AttnArgs {
   int* counter;
   int n_work;
   int expand;
-  int row_group;  // forward, dQ: sorted rows per group of the item order (see item_of)
+  int row_group;  // forward, dQ: sorted rows per group of the item order (see item_of); -1: seg_major_item
   int fwd_pair;   // forward: items are 128 rows of two query heads (1) or 256 rows of one (0)
   // dK/dV: units far longer than a share of the per-SM load, and the last
   // units of the cost order, are cut into chunks of 64-row steps; a chunk
