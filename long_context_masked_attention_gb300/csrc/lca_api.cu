@@ -993,7 +993,10 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     ph = phase_begin(3, sk);
     launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, sk);
     launch_sort(wl, sk);
-    launch_split_dkv(wl, usteps, sp, sms, sk);
+    // MHA with one mask map: whole units, key group by key group and head by
+    // head, so that the items in flight read one head's Q and dO
+    const bool dkv_seg_major = P.Hq == P.Hkv && P.hm_count == 1 && wl.expand > 1;
+    launch_split_dkv(wl, usteps, sp, sms, dkv_seg_major, sk);
     phase_end(ph, sk);
     if (fork) LCA_CUDA(cudaEventRecord(ev_planned, sk));
     AttnArgs a = base_args(c, dr);
@@ -1013,6 +1016,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.run_first = sp.run_first;
     a.run_of = sp.run_of;
     a.run_at = sp.run_at;
+    a.dkv_seg_major = dkv_seg_major ? 1 : 0;
     a.partials = reinterpret_cast<float*>(c.ws + c.L.k_part);
     a.n_units = static_cast<int>(k_units);
     a.nD = D;

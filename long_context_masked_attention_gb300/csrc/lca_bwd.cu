@@ -556,7 +556,23 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       w = __shfl_sync(0xFFFFFFFFu, w, 0);
       Item inf;
       inf.valid = 0;
-      if (w < n_work) {
+      if (w < n_work && a.dkv_seg_major) {
+        // whole units, key group by key group, head by head, key tile by key tile
+        const int kg = find_bucket(pv.kt_start, pv.n_kg, w / a.expand);
+        const int nk = pv.kt_start[kg + 1] - pv.kt_start[kg];
+        const int local = w - pv.kt_start[kg] * a.expand;
+        const int kt = local % nk;
+        const int unit = pv.kt_start[kg] + kt;  // one mask map: unit = key tile row
+        inf.valid = 1;
+        inf.kg = kg;
+        inf.kt = kt;
+        inf.rk = unit;
+        inf.g = local / nk;
+        inf.unit_hm = 0;
+        inf.begin = 0;
+        inf.nsteps = a.usteps[unit];
+        inf.slot = -1;
+      } else if (w < n_work) {
         // sorted unit i holding item w; its items are chunk-major, then KV head, so the
         // cost order (longest first) holds across heads and chunks
         int lo = 0, hi = n_runs;

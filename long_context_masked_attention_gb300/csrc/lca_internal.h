@@ -93,7 +93,9 @@ struct DkvSplit {
   int* run_at;       // per claim position: its run (runs by descending item cost)
   int max_slots;
 };
-void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st);
+// whole: no cuts (every unit one work item per KV head).
+void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, bool whole,
+                      cudaStream_t st);
 void launch_sort(const WorkList& wl, cudaStream_t st);
 void launch_materialize_seg(const PlanView& pv, int seg, int hm, long long cells, uint8_t* out, cudaStream_t st);
 void launch_tile_classes_seg(const PlanView& pv, int seg, int hm, int tiles, uint8_t* out, cudaStream_t st);
@@ -128,6 +130,9 @@ struct AttnArgs {
   int expand;
   int row_group;  // forward, dQ: sorted rows per group of the item order (see item_of); -1: seg_major_item
   int fwd_pair;   // forward: items are 128 rows of two query heads (1) or 256 rows of one (0)
+  // dK/dV: whole units taken key group by key group, head by head, key tile
+  // by key tile (MHA: the items in flight share a head's Q and dO in L2)
+  int dkv_seg_major;
   // dK/dV: units far longer than a share of the per-SM load, and the last
   // units of the cost order, are cut into chunks of 64-row steps; a chunk
   // writes f32 partial dV, dK that a reduction sums.

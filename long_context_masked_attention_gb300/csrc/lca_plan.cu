@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__
                                                          int* __restrict__ item_start,
                                                          int* __restrict__ split_start, int* __restrict__ n_work,
                                                          int* __restrict__ run_first, int* __restrict__ run_of,
-                                                         int* __restrict__ run_at) {
+                                                         int* __restrict__ run_at, int whole) {
   __shared__ long long red_ll[32];
   __shared__ int red[32];
   __shared__ int bucket_pos[kCostBuckets];
@@ -403,6 +403,10 @@ __global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__
   long long target = total * 3 / (4LL * max(1, num_sms));
   if (target < kMinChunkSteps * kCostDkv.full) target = kMinChunkSteps * kCostDkv.full;
   int tail = (num_sms + expand - 1) / expand;  // units holding the last num_sms items
+  if (whole) {  // no cuts: every unit is one work item per KV head
+    target = 1LL << 60;
+    tail = 0;
+  }
   const long long share = total / max(1, num_sms);
   const long long tail_min = max(static_cast<long long>(kMinChunkSteps) * kCostDkv.full, share / 4);
   for (int round = 0; round < 80; ++round) {  // shrink the cuts until the partial slots suffice
@@ -511,11 +515,12 @@ __global__ void __launch_bounds__(1024) split_dkv_kernel(const int* __restrict__
   }
 }
 
-void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, cudaStream_t st) {
+void launch_split_dkv(const WorkList& wl, const int* usteps, const DkvSplit& sp, int num_sms, bool whole,
+                      cudaStream_t st) {
   note_launches(1);
   split_dkv_kernel<<<1, 1024, 0, st>>>(wl.order, wl.cnt, usteps, wl.key, wl.n_sorted, wl.expand, num_sms,
                                        sp.max_slots, sp.nchunk, sp.item_start, sp.split_start, sp.n_work,
-                                       sp.run_first, sp.run_of, sp.run_at);
+                                       sp.run_first, sp.run_of, sp.run_at, whole ? 1 : 0);
 }
 
 // ---------------------------------------------------------------- cost sort
