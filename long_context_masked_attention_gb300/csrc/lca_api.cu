@@ -993,9 +993,11 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     ph = phase_begin(3, sk);
     launch_plan_dkv(c.V, tcls, wl, list_cnt, list_steps, usteps, sk);
     launch_sort(wl, sk);
-    // MHA with one mask map: whole units, key group by key group and head by
-    // head, so that the items in flight read one head's Q and dO
-    const bool dkv_seg_major = P.Hq == P.Hkv && P.hm_count == 1 && wl.expand > 1;
+    // One mask map and enough work items to balance without cuts (MHA, or at
+    // least eight items per SM): whole units, key group by key group and
+    // head by head, so that the items in flight read one head's Q and dO
+    const bool dkv_seg_major = P.hm_count == 1 && wl.expand > 1 &&
+                               (P.Hq == P.Hkv || k_units * wl.expand >= 8LL * sms);
     launch_split_dkv(wl, usteps, sp, sms, dkv_seg_major, sk);
     phase_end(ph, sk);
     if (fork) LCA_CUDA(cudaEventRecord(ev_planned, sk));
