@@ -333,6 +333,13 @@ lca_status validate(const lca_shape* sh, const lca_mask_desc* md, HostPlan& P) {
   return LCA_OK;
 }
 
+// Whether the call's K and V (bf16) exceed what L2 keeps for them: then the
+// query-major items in flight should cover a few heads of one segment
+// (seg_major_item), not every head of every segment as the cost order does.
+bool kv_beyond_l2(const HostPlan& P) {
+  return static_cast<long long>(P.Tk) * P.Hkv * kHeadDim * 2 * 2 > kKvL2Bytes;
+}
+
 Layout make_layout(const HostPlan& P, bool fwd, bool bwd) {
   Layout L;
   size_t o = 0;
@@ -838,10 +845,12 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(n_rows * wl.expand);
-    // MHA with segments of 8K rows or more on average: segment by segment,
-    // head by head (shorter segments keep the cost order, whose balance is
-    // worth more there: 2K and document batches were 10-13 % slower)
-    a.row_group = (P.Hq == P.Hkv && wl.expand > 1 && P.Tq >= 8192LL * std::max(1, P.n_seg)) ? -1 : 1;
+    // K/V larger than L2 and segments of 8K rows or more on average: segment
+    // by segment, head by head (shorter segments keep the cost order, whose
+    // balance is worth more there: 2K and document batches were 10-13 %
+    // slower; with K/V that fits in L2 the cost order is as local and
+    // balances better)
+    a.row_group = (wl.expand > 1 && kv_beyond_l2(P) && P.Tq >= 8192LL * std::max(1, P.n_seg)) ? -1 : 1;
     a.fwd_pair = P.fwd_pair ? 1 : 0;
     a.o = o;
     a.lse = lse;
@@ -1054,7 +1063,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.counter = wl.counter;
     a.expand = wl.expand;
     a.n_work = static_cast<int>(q_rows * wl.expand);
-    a.row_group = (P.Hq == P.Hkv && wl.expand > 1) ? -1 : 1;  // MHA: segment by segment, head by head
+    a.row_group = (wl.expand > 1 && kv_beyond_l2(P)) ? -1 : 1;  // K/V larger than L2: segment by segment, head by head
     a.nD = D;
     a.nlse2 = lse2;
     a.dq = dq;

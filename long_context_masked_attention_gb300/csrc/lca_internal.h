@@ -24,11 +24,13 @@ constexpr CostWeights kCostFwd{4, 10}, kCostDq{4, 5}, kCostDkv{4, 6};
 // A dK/dV chunk is at least this many 64-row steps long (a chunk pays a K/V
 // load and an epilogue, worth about ten steps).
 constexpr int kMinChunkSteps = 64;
-// With every query head on its own K/V (MHA) and one mask map, dQ items (and
-// forward items when the segments average 8K rows or more) go segment by
-// segment and head by head (seg_major_item), so the items in flight share
-// K/V in L2 instead of streaming every head's K/V from HBM (8K causal MHA:
-// forward and backward 10 % faster).
+// When a call's K/V exceed this many bytes (less than the 126 MB L2, which
+// also holds Q tiles and outputs), dQ items (and forward items when the
+// segments average 8K rows or more) go segment by segment and head by head
+// (seg_major_item), so the items in flight share K/V in L2 instead of
+// streaming every head's K/V from HBM (8K causal MHA: forward and backward
+// 10 % faster; 48K causal GQA forward 8 %).
+constexpr long long kKvL2Bytes = 96LL << 20;
 
 // Counts kernel launches made by this library (see lca_launch_count).
 void note_launches(int n);
