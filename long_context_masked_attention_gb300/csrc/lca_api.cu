@@ -853,6 +853,7 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     a.row_group = (wl.expand > 1 && kv_beyond_l2(P) && P.Tq >= 8192LL * std::max(1, P.n_seg)) ? -1 : 1;
     a.fwd_pair = P.fwd_pair ? 1 : 0;
     a.o = o;
+    a.out_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     a.lse = lse;
     a.prof = prof_slot(0, c.st);
     ph = phase_begin(1, c.st);
@@ -1034,6 +1035,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nlse2 = lse2;
     a.dk = dk;
     a.dv = dv;
+    a.out_v8 = ((reinterpret_cast<uintptr_t>(dk) | reinterpret_cast<uintptr_t>(dv)) & 31u) == 0;
     a.prof = prof_slot(1, sk);
     if (fork) LCA_CUDA(cudaStreamWaitEvent(sk, ev_pre, 0));  // -D and -LSE*log2(e)
     ph = phase_begin(4, sk);
@@ -1067,6 +1069,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     a.nD = D;
     a.nlse2 = lse2;
     a.dq = dq;
+    a.out_v8 = (reinterpret_cast<uintptr_t>(dq) & 31u) == 0;
     a.prof = prof_slot(2, c.st);
     // the dQ kernel is queued once dK/dV's lists are built, so both kernels
     // become ready together and the higher-priority dK/dV CTAs go first

@@ -49,13 +49,20 @@ __device__ __forceinline__ bool waitw(uint64_t* bar, uint32_t parity, const Attn
   return __all_sync(0xFFFFFFFFu, ok);
 }
 
-__device__ __forceinline__ uint4 pack8(const float* v, float mul) {
-  uint4 r;
-  r.x = pack_bf16x2(v[0] * mul, v[1] * mul);
-  r.y = pack_bf16x2(v[2] * mul, v[3] * mul);
-  r.z = pack_bf16x2(v[4] * mul, v[5] * mul);
-  r.w = pack_bf16x2(v[6] * mul, v[7] * mul);
-  return r;
+// 32 f32 values (TMEM words) times `mul` as 32 bf16 at p: two 32-byte stores
+// when the output is 32-byte aligned (v8), else four 16-byte ones.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, const uint32_t (&r)[32], float mul, bool v8) {
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * mul, __uint_as_float(r[2 * k + 1]) * mul);
+  if (v8) {
+    st_global_v8(p, w);
+    st_global_v8(p + 16, w + 8);
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      *reinterpret_cast<uint4*>(p + 8 * u) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+  }
 }
 
 // ====================================================================== dQ
@@ -406,19 +413,14 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       if (!waitw(&bar[B_DQFULL], items_done & 1, a, 133)) return;
       ++items_done;
       tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tbase + tl + 256 + half * 64 + 32 * c, r);
-        tmem_ld_wait();
-        if (valid) {
-          float f[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(qrow + 32 * c + 8 * u) = pack8(f + 8 * u, out_scale);
-        }
-      }
+      // the TMEM read of the second 32 columns overlaps the stores of the first
+      uint32_t r[2][32];
+      tmem_ld32(tbase + tl + 256 + half * 64, r[0]);
+      tmem_ld_wait();
+      tmem_ld32(tbase + tl + 256 + half * 64 + 32, r[1]);
+      if (valid) store_bf16x32(qrow, r[0], out_scale, a.out_v8);
+      tmem_ld_wait();
+      if (valid) store_bf16x32(qrow + 32, r[1], out_scale, a.out_v8);
     } else if (valid) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(qrow + 8 * u) = make_uint4(0, 0, 0, 0);
@@ -946,39 +948,25 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
         tmem_ld32(tbase + tl + 256 + half * 64 + 32 * c, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(pdv + 32 * c + 4 * u) = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) st_global_v8(pdv + 32 * c + 8 * u, r + 8 * u);
         tmem_ld32(tbase + tl + 384 + half * 64 + 32 * c, r);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(pdk + 32 * c + 4 * u) = make_uint4(r[4 * u], r[4 * u + 1], r[4 * u + 2], r[4 * u + 3]);
+        for (int u = 0; u < 4; ++u) st_global_v8(pdk + 32 * c + 8 * u, r + 8 * u);
       }
     } else if (inf.nsteps > 0) {
       if (!waitw(&bar[B_ACCFULL], acc_items & 1, a, 233)) return;
       ++acc_items;
       tc_fence_after();
+      // each TMEM read of 32 columns overlaps the stores of the previous ones
+      uint32_t r[2][32];
+      tmem_ld32(tbase + tl + 256 + half * 64, r[0]);
+      tmem_ld_wait();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        float f[32];
-        tmem_ld32(tbase + tl + 256 + half * 64 + 32 * c, r);
-        tmem_ld_wait();
-        if (valid) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) *reinterpret_cast<uint4*>(dV + orow + 32 * c + 8 * u) = pack8(f + 8 * u, dv_scale);
-        }
-        tmem_ld32(tbase + tl + 384 + half * 64 + 32 * c, r);
-        tmem_ld_wait();
-        if (valid) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-            *reinterpret_cast<uint4*>(dK + orow + 32 * c + 8 * u) = pack8(f + 8 * u, dk_scale);
-        }
+      for (int c = 0; c < 4; ++c) {  // dV columns 0-31, 32-63, then dK
+        if (c < 3) tmem_ld32(tbase + tl + 256 + 128 * ((c + 1) >> 1) + half * 64 + 32 * ((c + 1) & 1), r[(c + 1) & 1]);
+        if (valid) store_bf16x32((c < 2 ? dV : dK) + orow + 32 * (c & 1), r[c & 1], c < 2 ? dv_scale : dk_scale, a.out_v8);
+        if (c < 3) tmem_ld_wait();
       }
     } else if (valid) {
 #pragma unroll

@@ -553,21 +553,27 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       float inv = (l > 0.f) ? 1.f / l : 0.f;
       if (kDrop) inv *= a.drop_inv;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tO + 32 * c, r);
-        tmem_ld_wait();
-        if (valid) {
+      uint32_t r[2][32];
+      tmem_ld32(tO, r[0]);
+      tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * u + 0]) * inv, __uint_as_float(r[8 * u + 1]) * inv);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * u + 2]) * inv, __uint_as_float(r[8 * u + 3]) * inv);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * u + 4]) * inv, __uint_as_float(r[8 * u + 5]) * inv);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * u + 6]) * inv, __uint_as_float(r[8 * u + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) = v;
+      for (int c = 0; c < 4; ++c) {
+        if (c < 3) tmem_ld32(tO + 32 * (c + 1), r[(c + 1) & 1]);
+        if (valid) {
+          uint32_t w[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_bf16x2(__uint_as_float(r[c & 1][2 * k]) * inv, __uint_as_float(r[c & 1][2 * k + 1]) * inv);
+          if (a.out_v8) {
+            st_global_v8(orow + 32 * c, w);
+            st_global_v8(orow + 32 * c + 16, w + 8);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * u) = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
           }
         }
+        if (c < 3) tmem_ld_wait();
       }
     } else if (valid) {
 #pragma unroll

@@ -161,6 +161,7 @@ struct AttnArgs {
   PhiloxKeys drop_keys;
   // tensors
   void* o;
+  int out_v8;  // the kernel's bf16 outputs are 32-byte aligned: rows are written in 32-byte stores
   float* lse;
   const float* nD;     // -D (times the keep probability under dropout), [Hq][Tq]
   const float* nlse2;  // -LSE * log2(e), [Hq][Tq]

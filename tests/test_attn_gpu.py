@@ -67,6 +67,39 @@ def test_repeated_calls_are_deterministic(lca):
         assert np.array_equal(to_np(a), to_np(b))
 
 
+@pytest.mark.parametrize("which", [5, 2])
+def test_outputs_16_byte_aligned(lca, which):
+    """Outputs that are 16- but not 32-byte aligned take 16-byte row stores
+    instead of 32-byte ones: parity with the oracle, and the same bits as
+    outputs at a 32-byte boundary (forward O; backward dQ, dK, dV)."""
+    import torch
+
+    prob = cases.gpu_small_all()[which]
+    q, k, v, do = (t.cuda() for t in make_tensors(prob))
+    segs, mask, sc = prob.segments, prob.mask, prob.scale
+    o, lse = lca.attn_fwd(q, k, v, segs, mask, sc)
+    grads = lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc)
+
+    def off16(t):
+        buf = torch.full((t.numel() + 8,), 7.0, dtype=t.dtype, device="cuda")
+        u = buf[8:].view(t.shape)
+        assert t.data_ptr() % 32 == 0 and u.data_ptr() % 32 == 16
+        return u
+
+    o16 = off16(o)
+    lca.attn_fwd(q, k, v, segs, mask, sc, out=o16)
+    g16 = [off16(g) for g in grads]
+    lca.attn_bwd(do, q, k, v, o, lse, segs, mask, sc, dq=g16[0], dk=g16[1], dv=g16[2])
+    torch.cuda.synchronize()
+    assert torch.equal(o16, o)
+    for a, b in zip(g16, grads):
+        assert torch.equal(a, b)
+    O, L = oracle.attention_forward(prob, *(t.cpu() for t in (q, k, v)))
+    check_fwd(o16, lse, O, L, what=prob.name + "_o16")
+    refs = oracle.attention_backward(prob, *(t.cpu() for t in (q, k, v, do)))
+    check_bwd(g16, refs, what=prob.name + "_g16")
+
+
 def test_status_word_clean_after_calls(lca):
     import torch
 
