@@ -89,10 +89,14 @@ enum : int {
   B_ITFULL, B_ITEMPTY = B_ITFULL + 2, B_DRAIN = B_ITEMPTY + 2, B_COUNT
 };
 
+// 64 bytes; the segment's descriptor and the first list entry travel with
+// the item, so the compute warps start an item without a global load
 struct Item {
-  int valid, seg, qt, head, hm, cnt;
+  int valid, e0, qt, head, hm, cnt;
   long long ebase;
+  SegInfo sg;
 };
+static_assert(sizeof(Item) == 64, "two items fill the 128 bytes between the barriers and the TMEM slot");
 
 // `counts` (shared memory) receives the CTA's work items and its full and
 // partial key tiles, for the optional per-CTA profile.
@@ -125,13 +129,14 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         const int hm = row / pv.R128, rr = row % pv.R128;
         const int s = find_bucket(pv.q128_start, pv.n_seg, rr);
         inf.valid = 1;
-        inf.seg = s;
+        inf.sg = pv.segs[s];
         inf.qt = rr - pv.q128_start[s];
         inf.hm = hm;
         inf.head = (pv.hm_count == 1) ? head : hm;
         inf.cnt = a.cnt[row];
-        inf.ebase = hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(inf.qt) * pv.segs[s].nk;
+        inf.ebase = hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(inf.qt) * inf.sg.nk;
       }
+      inf.e0 = (inf.valid && inf.cnt > 0) ? static_cast<int>(entries[inf.ebase]) : 0;
       items[slot] = inf;
       mbar_arrive(&bar[B_ITFULL + slot]);
       if (!inf.valid) {
@@ -141,7 +146,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         return;
       }
       ++n_items;
-      const SegInfo sg = pv.segs[inf.seg];
+      const SegInfo sg = inf.sg;
       if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 111)) goto abort;
       mbar_arrive_expect_tx(&bar[B_QFULL], 2 * kTile128);
       const int y0 = sg.q_off + inf.qt * kTile;
@@ -151,7 +156,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       }
       q_issued = it + 1;
       const int g = inf.head / pv.G;
-      uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
+      uint32_t e_next = static_cast<uint32_t>(inf.e0);
       for (int t = 0; t < inf.cnt; ++t, ++tiles) {
         const uint32_t e = e_next;
         if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
@@ -285,6 +290,13 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
     if (!inf.valid) return;
+    // the row's statistics are loaded while the dO rows are copied
+    const SegInfo sg = inf.sg;
+    const int i = inf.qt * kTile + row;
+    const bool valid = i < sg.q_len;
+    const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
+    const float nl2v = valid ? a.nlse2[stat] : -INFINITY;
+    const float nDv = valid ? a.nD[stat] : 0.f;
     if (inf.cnt > 0) {
       // this item's dO rows into TMEM, the A operand of dP = dO V^T: thread
       // (row, half) copies the row's 64 columns of its half from the
@@ -308,15 +320,10 @@ __device__ __forceinline__ void compute(const AttnArgs& a, uint8_t* sm, uint64_t
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[B_DOFULL]);
     }
-    const SegInfo sg = pv.segs[inf.seg];
-    const int i = inf.qt * kTile + row;
-    const bool valid = i < sg.q_len;
     const Span row_sp = row_mask_ctx(pv.mask, sg, i);  // the row's span or query block, for every tile
-    const size_t stat = static_cast<size_t>(inf.head) * pv.Tq + sg.q_off + i;
-    const uint64_t nl2 = f2(valid ? a.nlse2[stat] : -INFINITY, valid ? a.nlse2[stat] : -INFINITY);  // -LSE2, twice
-    const float nDv = valid ? a.nD[stat] : 0.f;
+    const uint64_t nl2 = f2(nl2v, nl2v);  // -LSE2, twice
     const uint64_t nD2 = f2(nDv, nDv);
-    uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
+    uint32_t e_next = static_cast<uint32_t>(inf.e0);
     for (int t = 0; t < inf.cnt; ++t, ++tiles) {
       const uint32_t e = e_next;  // the next entry's load overlaps this tile's work
       if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];

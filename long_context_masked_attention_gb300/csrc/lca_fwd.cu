@@ -67,10 +67,15 @@ enum : int {
   B_COUNT = B_DRAIN + 1
 };
 
-struct Item {  // 32 bytes, broadcast from the producer to the other roles
-  int valid, seg, qb, head, hm, cnt;
+// 64 bytes, broadcast from the producer to the other roles; the segment's
+// descriptor and the first list entry travel with the item, so the softmax
+// warps start an item without a global load
+struct Item {
+  int valid, e0, qb, head, hm, cnt;
   long long ebase;
+  SegInfo sg;
 };
+static_assert(sizeof(Item) == 64, "two items fill the 128 bytes between the barriers and the TMEM slot");
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);  // S = Q K^T (both K-major)
 constexpr uint32_t kIdescO = idesc_bf16_f32(128, 128, false, true);   // O += P V (P in TMEM, V N-major)
@@ -125,7 +130,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         const int hm = row / R, rr = row % R;
         const int s = find_bucket(qstart, pv.n_seg, rr);
         inf.valid = 1;
-        inf.seg = s;
+        inf.sg = pv.segs[s];
         inf.qb = rr - qstart[s];
         inf.hm = hm;
         inf.head = (pv.hm_count == 1) ? (a.fwd_pair ? 2 * head : head) : hm;
@@ -133,6 +138,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
         inf.ebase = a.fwd_pair ? hm * pv.dq_per_hm + pv.dq_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk
                                : hm * pv.fwd_per_hm + pv.fwd_off[s] + static_cast<long long>(inf.qb) * pv.segs[s].nk;
       }
+      inf.e0 = (inf.valid && inf.cnt > 0) ? static_cast<int>(entries[inf.ebase]) : 0;
       items[slot] = inf;
       mbar_arrive(&bar[B_ITFULL + slot]);
       if (!inf.valid) {
@@ -143,7 +149,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
       }
       ++n_items;
 
-      const SegInfo sg = pv.segs[inf.seg];
+      const SegInfo sg = inf.sg;
       if (it >= 1 && !wait1(&bar[B_QEMPTY], (it - 1) & 1, a, 11)) goto abort;
       mbar_arrive_expect_tx(&bar[B_QFULL], 2 * kTileBytes);
       const int y0 = sg.q_off + inf.qb * (a.fwd_pair ? 1 : 2) * kTile;
@@ -157,7 +163,7 @@ __device__ __forceinline__ void producer(const AttnArgs& a, const CUtensorMap* t
 
       const int g = inf.head / pv.G;
       const int n = inf.cnt;
-      uint32_t e_next = (n > 0) ? entries[inf.ebase] : 0u;
+      uint32_t e_next = static_cast<uint32_t>(inf.e0);
       for (int t = 0; t < n; ++t) {
         const uint32_t e = e_next;
         if (t + 1 < n) e_next = entries[inf.ebase + t + 1];
@@ -210,7 +216,7 @@ __device__ __forceinline__ void mma_issuer(const AttnArgs& a, uint8_t* sQ, uint8
       tc_fence_after();
       const int n = inf.cnt;
       bool first_pv[2] = {true, true};
-      uint32_t e_cur = (n > 0) ? entries[inf.ebase] : 0u, e_prev = 0u;
+      uint32_t e_cur = static_cast<uint32_t>(inf.e0), e_prev = 0u;
       for (int t = 0; t <= n; ++t) {
         const uint32_t e_nxt = (t + 1 < n) ? entries[inf.ebase + t + 1] : 0u;
         const uint32_t vidx = kv_iter + v_load_index(t - 1), kidx = kv_iter + k_load_index(t);
@@ -461,7 +467,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
     __syncwarp();
     if (lane == 0) mbar_arrive(&bar[B_ITEMPTY + slot]);
     if (!inf.valid) return;
-    const SegInfo sg = pv.segs[inf.seg];
+    const SegInfo sg = inf.sg;
     // row inside the segment and query head of this sub-tile
     const int i = a.fwd_pair ? inf.qb * kTile + row : inf.qb * 2 * kTile + x * kTile + row;
     const int head = inf.head + (a.fwd_pair ? x : 0);
@@ -469,7 +475,7 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
     const Span row_sp = row_mask_ctx(pv.mask, sg, i);  // the row's span or query block, for every tile
     float m_use = -INFINITY, l = 0.f;
     bool any = false;
-    uint32_t e_next = (inf.cnt > 0) ? entries[inf.ebase] : 0u;
+    uint32_t e_next = static_cast<uint32_t>(inf.e0);
     for (int t = 0; t < inf.cnt; ++t) {
       const uint32_t e = e_next;  // the next entry's load overlaps this tile's work
       if (t + 1 < inf.cnt) e_next = entries[inf.ebase + t + 1];
