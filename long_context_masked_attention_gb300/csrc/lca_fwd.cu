@@ -558,7 +558,6 @@ __device__ __forceinline__ void softmax_wg(const AttnArgs& a, int x, uint64_t* b
       tc_fence_after();
       float inv = (l > 0.f) ? 1.f / l : 0.f;
       if (kDrop) inv *= a.drop_inv;
-#pragma unroll
       uint32_t r[2][32];
       tmem_ld32(tO, r[0]);
       tmem_ld_wait();
