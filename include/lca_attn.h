@@ -148,14 +148,19 @@ LCA_API lca_status lca_workspace_size(const lca_shape* shape, const lca_mask_des
 
 /* Forward (FlashAttention-2 核心优化: Q-split work, deferred rescale, one LSE
  * per row).  q, k, v: device bf16 inputs; o: bf16 [Tq][Hq][d] output;
- * lse: float [Hq][Tq] output (outputs in device or mapped host memory). */
+ * lse: float [Hq][Tq] output (outputs in device or mapped host memory).
+ * q, k, v and o must be 16-byte aligned and lse 4-byte aligned
+ * (LCA_ERR_INVALID_ARG otherwise); an o that is 32-byte aligned is written
+ * with 32-byte stores, any other with 16-byte ones (same values). */
 LCA_API lca_status lca_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, const lca_shape* shape,
                         const lca_mask_desc* mask, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward (FlashAttention-2 核心优化, 反向传播: dK/dV per key tile, dQ in a
  * separate query-tile pass, D = rowsum(dO * O) prepass).  dout, q, k, v, o:
  * device bf16; lse: device float from lca_attn_fwd; dq, dk, dv: bf16 outputs
- * in device or mapped host memory (written, not accumulated).
+ * in device or mapped host memory (written, not accumulated).  Every bf16
+ * pointer must be 16-byte aligned (LCA_ERR_INVALID_ARG otherwise); dq, and
+ * dk with dv, are written with 32-byte stores when 32-byte aligned.
  * The dK/dV pass runs on a stream the library owns (one per device, highest
  * priority), forked from `stream` and joined back to it with events, so that
  * the dQ pass runs beside it; all of the call's work still comes after the

@@ -810,7 +810,8 @@ lca_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, f
     if (!o || !lse) return LCA_ERR_INVALID_ARG;
   }
   if (P.Tk > 0 && (!device_input(k) || !device_input(v))) return LCA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LCA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return LCA_ERR_INVALID_ARG;
   const long long n_rows = static_cast<long long>(P.hm_count) * (P.fwd_pair ? P.R128 : P.R256);
   CUtensorMap tq, tk, tv;
   if (n_rows > 0) {
@@ -929,7 +930,7 @@ lca_status attn_bwd_impl(const void* dout, const void* q, const void* k, const v
     if (!dk || !dv) return LCA_ERR_INVALID_ARG;
   }
   if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dq) ||
-      !aligned16(dk) || !aligned16(dv))
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return LCA_ERR_INVALID_ARG;
   const long long q_rows = static_cast<long long>(P.hm_count) * P.R128;
   const int hkv_m = (P.hm_count == 1) ? 1 : P.Hkv;

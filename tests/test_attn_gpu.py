@@ -100,6 +100,35 @@ def test_outputs_16_byte_aligned(lca, which):
     check_bwd(g16, refs, what=prob.name + "_g16")
 
 
+def test_misaligned_lse_refused_before_launch(lca):
+    """An LSE pointer that is not 4-byte aligned (the row statistics are f32)
+    makes both calls return LCA_ERR_INVALID_ARG with nothing launched."""
+    import ctypes as C
+
+    import torch
+
+    prob = cases.gpu_small_all()[1]
+    q, k, v, do = (t.cuda() for t in make_tensors(prob))
+    call = lca.marshal(prob.Tq, prob.Tk, prob.Hq, prob.Hkv, prob.d, prob.segments, prob.mask, prob.scale)
+    ws = torch.empty(max(lca.workspace_size(call, True), 256), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(q)
+    lse_buf = torch.empty(prob.Hq * prob.Tq + 1, dtype=torch.float32, device="cuda")
+    bad = lse_buf.data_ptr() + 2
+    lib = lca.binding.load()
+    torch.cuda.synchronize()
+    n0 = lib.lca_launch_count()
+    st = lib.lca_attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), bad, C.byref(call.shape),
+                          C.byref(call.mask), ws.data_ptr(), ws.numel(), None)
+    assert st == 1
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st = lib.lca_attn_bwd(do.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), bad,
+                          dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), C.byref(call.shape), C.byref(call.mask),
+                          ws.data_ptr(), ws.numel(), None)
+    assert st == 1
+    assert lib.lca_launch_count() == n0
+    torch.cuda.synchronize()
+
+
 def test_status_word_clean_after_calls(lca):
     import torch
 
