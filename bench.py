@@ -561,6 +561,23 @@ def run_ours(args):
         host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (q, lse, q, k, v)] for _ in probs]
         h2d = sum(t.numel() * t.element_size() for t in hosts_in)
         d2h = sum(t.numel() * t.element_size() for outs in host_out for t in outs)
+        # the copy rates of these very buffers, alone, just before the timed
+        # region: the leg can only hide its copies when they run near the
+        # host link's rate (pinned pages of a VM whose host memory has been
+        # churned sometimes copy at well under it)
+        link = {}
+        for name, pairs in (("d2h", [(dst, src) for i in range(len(probs)) for src, dst in zip(dev_out[i], host_out[i])]),
+                            ("h2d", list(zip(dev_in[0], hosts_in)))):
+            nbytes = sum(dst.numel() * dst.element_size() for dst, _ in pairs)
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(copy):
+                a_ev.record(copy)
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+                b_ev.record(copy)
+            torch.cuda.synchronize()
+            link[name] = round(nbytes / (a_ev.elapsed_time(b_ev) * 1e-3) / 1e9, 1)
         ev_in_ready = [torch.cuda.Event() for _ in range(2)]
         ev_in_free = [torch.cuda.Event() for _ in range(2)]
         ev_out_ready = [torch.cuda.Event() for _ in probs]
@@ -611,6 +628,7 @@ def run_ours(args):
         e2e = {"value": e_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
                "outputs": args.e2e_outputs,
+               "copy_gbps_alone": link,
                "host_binding": ({"cpus": len(local_cpus), "gpu_numa_node": numa_node} if bound else
                                 "not bound (GPU's local CPUs unknown)"),
                "copies": ("inputs on one copy stream, double-buffered across steps; dQ, dK, dV stored by the "
